@@ -1,0 +1,81 @@
+// Device helpers shared by the kernels of the fused-MoE hot path (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+constexpr int kGroup = 128;  // 1x128 activation groups, 128x128 weight blocks
+
+// Kernel launches made by this library (read by moe_kernel_launch_count()).
+void note_launches(int n);
+
+// Launch-status helper: returns MOE_ERR_CUDA if the last launch failed.
+inline int launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// Round-to-nearest-even fp32 -> bf16 bits (the hardware conversion).
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// Two fp32 -> two e4m3 codes (low byte = a), round-to-nearest-even, saturating to
+// +-448 (cvt.rn.satfinite.e4m3x2.f32).
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Local expert of a top-k id; -1 when dropped. Bad ids (outside [-1, E)) bump *bad.
+__device__ __forceinline__ int local_expert(int id, const int32_t* __restrict__ expert_map, int E, int El, int& bad) {
+    if (id == -1) return -1;
+    if (id < 0 || id >= E) {
+        ++bad;
+        return -1;
+    }
+    int l = expert_map ? __ldg(expert_map + id) : id;
+    return (l >= 0 && l < El) ? l : -1;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Quantise 16 consecutive fp32 values of one 1x128 group (8 lanes x 16 values, the 8
+// lanes aligned on a multiple of 8 within the warp) to e4m3 with the group's fp32 scale
+// amax/448. Returns the 16 codes packed in a uint4 and the scale.
+__device__ __forceinline__ uint4 quant16_group8(const float (&v)[16], float& scale_out) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = __fdiv_rn(amax, 448.0f);
+    scale_out = s;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint16_t lo, hi;
+        if (s == 0.f) {
+            lo = hi = 0;
+        } else {
+            lo = f32x2_to_e4m3x2(__fdiv_rn(v[4 * i + 0], s), __fdiv_rn(v[4 * i + 1], s));
+            hi = f32x2_to_e4m3x2(__fdiv_rn(v[4 * i + 2], s), __fdiv_rn(v[4 * i + 3], s));
+        }
+        w[i] = uint32_t(lo) | (uint32_t(hi) << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+}  // namespace moe

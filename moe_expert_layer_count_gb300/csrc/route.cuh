@@ -1,0 +1,34 @@
+// Host-side launchers of the HBM-bound kernels (route.cu) and the grouped GEMM.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kScatterThreads = 256;   // 8 warps per CTA in the scatter index kernels
+constexpr int kScatterMinSlots = 2048; // top-k slots per CTA at least
+constexpr int kMaxScatterCtas = 256;   // at most this many CTAs rank the slots
+constexpr int kMaxLocalExperts = 1024;
+
+int scatter_slots_per_cta(int64_t n);
+
+int launch_count(const int32_t* ids, int64_t n, const int32_t* expert_map, int E, int El, int32_t* counts,
+                 int32_t* err_count, int num_sms, cudaStream_t stream);
+
+int launch_scatter(const uint16_t* x, int64_t M, int K, const int32_t* ids, const float* topk_weights, int topk,
+                   const int32_t* expert_map, int E, int El, const int32_t* counts, int apply_on_input, int quant,
+                   void* a_out, float* a_scale, int32_t* expert_offsets, int32_t* src2dst, int32_t* hist,
+                   cudaStream_t stream);
+
+int launch_gather(const uint16_t* y, const int32_t* src2dst, const float* topk_weights, int64_t M, int topk, int K,
+                  int apply_on_input, uint16_t* out, cudaStream_t stream);
+
+int launch_silu_mul_quant(const float* c1, const int32_t* expert_offsets, int El, int64_t rp_cap, int N, uint8_t* h,
+                          float* h_scale, cudaStream_t stream);
+
+int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
+                        const int32_t* expert_offsets, int El, int64_t rp_cap, int n_out, int k_in, int epilogue,
+                        void* out, float* out_scale, int num_sms, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,70 @@
+"""The C-ABI library builds, loads and exports every symbol of include/*.h, and its
+host-side queries and argument checks behave as documented. No kernel is launched."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    import moe_expert_layer_count_gb300 as moe
+    return moe.lib()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names |= set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert {"moe_count_expert_tokens", "moe_scatter", "moe_grouped_gemm_fp8", "moe_silu_mul_quant",
+            "moe_gather_weight_reduce", "moe_forward_chunked"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_binding_declares_every_symbol(L):
+    import moe_expert_layer_count_gb300 as moe
+    assert declared_symbols() <= set(moe.SIGNATURES)
+
+
+def test_size_queries(L):
+    import moe_expert_layer_count_gb300 as moe
+    import oracle
+    for Mc, topk, El in ((1, 8, 64), (128, 8, 64), (64, 8, 128), (8192, 8, 128), (3, 2, 1), (0, 8, 4)):
+        assert moe.moe_rp_cap(Mc, topk, El) == oracle.rp_cap(Mc, topk, El)
+    assert moe.moe_rp_cap(1, 0, 4) == -1
+    assert moe.moe_workspace_size(128, 2048, 768, 8, 64) > 0
+    assert moe.moe_workspace_size(128, 2000, 768, 8, 64) == 0          # K not a multiple of 128
+    # per-chunk sizing: a smaller chunk never needs more
+    assert moe.moe_workspace_size(1, 2048, 768, 8, 64) < moe.moe_workspace_size(128, 2048, 768, 8, 64)
+    assert moe.status_string(0) == "ok"
+
+
+def test_argument_checks_return_before_any_launch(L):
+    # invalid arguments are refused on the host: nothing touches a device
+    p = ctypes.c_void_p(16)
+    assert L.moe_count_expert_tokens(p, 4, 0, None, 8, 8, p, None, None) == 1          # topk 0
+    assert L.moe_count_expert_tokens(p, 4, 2, None, 8, 0, p, None, None) == 1          # El 0
+    assert L.moe_count_expert_tokens(p, 4, 2, None, 8, 2000, p, None, None) == 1       # El > 1024
+    assert L.moe_gather_weight_reduce(p, p, p, 4, 2, 100, 0, p, None) == 1             # K % 128
+    assert L.moe_grouped_gemm_fp8(p, p, p, p, p, 4, 128, 384, 256, 2, p, p, None) == 1  # silu needs n_out%256
+    assert L.moe_silu_mul_quant(None, p, 4, 128, 128, p, p, None) == 1
+    ws = ctypes.c_void_p(4096)
+    # out overlapping the workspace is refused
+    assert L.moe_forward_chunked(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 4, 0, ws,
+                                 ws, 1 << 30, None, None) == 1
+    # workspace too small
+    assert L.moe_forward_chunked(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 4, 0, p,
+                                 ws, 16, None, None) == 2

@@ -1,0 +1,198 @@
+"""GPU parity of the grouped FP8 GEMM and of the whole chunked layer against the CPU
+oracle, through the C ABI, from tiny cases to the full-size workloads the benchmark
+times (sampled tokens there)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_count_gb300 as moe
+import moe_inputs as mi
+import oracle
+from helpers import dev, host, host_bits, layer_tolerance, e4m3_ulp_diff
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def permuted_inputs(counts, K, seed):
+    """Random FP8 activations laid out in 128-aligned expert blocks (padding rows hold
+    random codes too: they must not disturb the kept rows)."""
+    rng = np.random.default_rng(seed)
+    counts = np.array(counts, np.int32)
+    offs = oracle.offsets(counts)
+    R = int(offs[-1])
+    x = (rng.standard_normal((max(R, 1), K)) * rng.uniform(0.05, 8, (max(R, 1), 1))).astype(np.float32)
+    A, SA = oracle.quant_rows(x)
+    return counts, offs, A[:R], SA[:R]
+
+
+def kept_rows(offs, counts):
+    return np.concatenate([np.arange(offs[l], offs[l] + counts[l]) for l in range(len(counts))] + [np.zeros(0, int)])
+
+
+@pytest.mark.parametrize("counts,n_out,k_in", [([5, 0, 130], 256, 384), ([128], 128, 128),
+                                               ([1, 300, 17, 0, 0, 64], 512, 768), ([200] * 3, 2048, 768)])
+@pytest.mark.parametrize("epi", [moe.MOE_EPI_F32, moe.MOE_EPI_BF16])
+def test_grouped_gemm_matches_oracle(counts, n_out, k_in, epi):
+    counts, offs, A, SA = permuted_inputs(counts, k_in, seed=n_out + k_in)
+    El = len(counts)
+    W, S = mi.expert_weights(El, n_out, k_in, seed=7, stream=1)
+    S = S * np.random.default_rng(3).uniform(0.5, 2.0, S.shape).astype(np.float32)
+    out = moe.moe_grouped_gemm_fp8(dev(A), dev(SA), dev(W), dev(S), dev(offs), epi)
+    torch.cuda.synchronize()
+    C = oracle.grouped_gemm(A, SA, W, S, offs, counts)
+    rows = kept_rows(offs, counts)
+    ref = C[rows]
+    got = host(out)[rows] if epi == moe.MOE_EPI_F32 else mi.bf16_to_f32(host_bits(out)[rows]).astype(np.float64)
+    tol = 1e-5 if epi == moe.MOE_EPI_F32 else 8e-3
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all()
+    assert err.max() <= tol * np.abs(ref).max(), err.max() / np.abs(ref).max()
+
+
+def test_grouped_gemm_identity_weights_bit_exact():
+    """W = block-diagonal 1.0, scale 1: each output is a single product, no summation
+    order freedom, so the fp32 results equal the oracle's exactly."""
+    K = 256
+    counts, offs, A, SA = permuted_inputs([5, 0, 130], K, seed=1)
+    El = 3
+    W = np.zeros((El, K, K), np.uint8)
+    for l in range(El):
+        np.fill_diagonal(W[l], 0x38)
+    S = np.ones((El, 2, 2), np.float32)
+    out = moe.moe_grouped_gemm_fp8(dev(A), dev(SA), dev(W), dev(S), dev(offs), moe.MOE_EPI_F32)
+    torch.cuda.synchronize()
+    C = oracle.grouped_gemm(A, SA, W, S, offs, counts).astype(np.float32)
+    rows = kept_rows(offs, counts)
+    assert (host(out)[rows].view(np.uint32) == C[rows].view(np.uint32)).all()
+
+
+def to_dev_layer(li):
+    return dict(x=dev(li.x), ids=dev(li.topk_ids), w=dev(li.topk_weights), w13=dev(li.w13),
+                s13=dev(li.w13_scale), w2=dev(li.w2), s2=dev(li.w2_scale),
+                m=None if li.expert_map is None else dev(li.expert_map))
+
+
+def gpu_forward(d, E, chunk=None, apply_on_input=False):
+    out = moe.moe_forward_chunked(d["x"], d["ids"], d["w"], d["w13"], d["s13"], d["w2"], d["s2"], E,
+                                  expert_map=d["m"], chunk_size=chunk, apply_router_weight_on_input=apply_on_input)
+    torch.cuda.synchronize()
+    return host_bits(out)
+
+
+def oracle_forward(li, chunk=None, apply_on_input=False):
+    return oracle.forward_chunked(li.x, li.topk_ids, li.topk_weights, li.w13, li.w13_scale, li.w2, li.w2_scale,
+                                  li.wl.E, expert_map=li.expert_map, chunk_size=chunk,
+                                  apply_router_weight_on_input=apply_on_input)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    li = mi.make_layer_inputs(mi.TINY)
+    return li, to_dev_layer(li)
+
+
+@pytest.mark.parametrize("apply_on_input", [False, True])
+def test_tiny_layer(tiny, apply_on_input):
+    li, d = tiny
+    got = gpu_forward(d, li.wl.E, apply_on_input=apply_on_input)
+    ref = oracle_forward(li, apply_on_input=apply_on_input)
+    layer_tolerance(got, ref)
+
+
+def test_tiny_layer_chunk_sizes_bit_identical(tiny):
+    li, d = tiny
+    full = gpu_forward(d, li.wl.E)
+    for chunk in (1, 7, 63, 64, 1000):
+        assert (gpu_forward(d, li.wl.E, chunk=chunk) == full).all(), chunk
+
+
+def test_tiny_layer_local_experts(tiny):
+    li, d = tiny
+    E = li.wl.E
+    m = mi.random_expert_map(E, 3, seed=5)
+    sel = np.nonzero(m >= 0)[0]
+    d2 = dict(d, m=dev(m), w13=dev(li.w13[sel]), s13=dev(li.w13_scale[sel]), w2=dev(li.w2[sel]),
+              s2=dev(li.w2_scale[sel]))
+    got = gpu_forward(d2, E, chunk=10)
+    ref = oracle.forward_chunked(li.x, li.topk_ids, li.topk_weights, li.w13[sel], li.w13_scale[sel], li.w2[sel],
+                                 li.w2_scale[sel], E, expert_map=m, chunk_size=10)
+    layer_tolerance(got, ref)
+    # tokens with no local expert give zero rows
+    none_local = ~(m[li.topk_ids] >= 0).any(axis=1)
+    assert (mi.bf16_to_f32(got[none_local]) == 0).all()
+
+
+def test_layer_no_local_expert_is_zero(tiny):
+    li, d = tiny
+    E = li.wl.E
+    m = np.full(E, -1, np.int32)
+    d2 = dict(d, m=dev(m))
+    got = gpu_forward(d2, E)
+    assert (mi.bf16_to_f32(got) == 0).all()
+
+
+@pytest.fixture(scope="module")
+def decode():
+    li = mi.make_layer_inputs(mi.QWEN3_DECODE)
+    return li, to_dev_layer(li)
+
+
+def test_qwen3_decode_layer(decode):
+    li, d = decode
+    got = gpu_forward(d, li.wl.E)
+    ref = oracle_forward(li)
+    layer_tolerance(got, ref)
+
+
+def sampled_tokens(M, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, M - 1], rng.choice(M, n, replace=False)]))
+
+
+def check_full_size(li, chunk, n_samples):
+    """The benchmark's launch configuration at full size: routing/permutation/FP8
+    activations bit-exact over the first chunk, layer output on sampled tokens."""
+    wl = li.wl
+    d = to_dev_layer(li)
+    got = gpu_forward(d, wl.E, chunk=chunk)
+    assert np.isfinite(mi.bf16_to_f32(got)).all()
+    toks = sampled_tokens(wl.M, n_samples, wl.seed)
+    ref = oracle.forward_tokens(toks, li.x, li.topk_ids, li.topk_weights, li.w13, li.w13_scale, li.w2,
+                                li.w2_scale, wl.E, expert_map=li.expert_map)
+    layer_tolerance(got[toks], ref)
+    # first chunk: counts, offsets, src2dst and FP8 activations vs the oracle
+    Mc = min(chunk or wl.M, wl.M)
+    El = wl.El
+    ids = d["ids"][:Mc].contiguous()
+    counts = moe.moe_count_expert_tokens(ids, wl.E, El, d["m"])
+    a, sa, offs, s2d = moe.moe_scatter(d["x"][:Mc].contiguous(), ids, d["w"][:Mc].contiguous(), wl.E, El, counts,
+                                       d["m"])
+    torch.cuda.synchronize()
+    r = oracle.scatter(li.x[:Mc], li.topk_ids[:Mc], li.topk_weights[:Mc], wl.E, El, li.expert_map)
+    assert (host(counts) == r["counts"]).all()
+    assert (host(offs) == r["offsets"]).all()
+    assert (host(s2d) == r["src2dst"]).all()
+    rows = r["src2dst"].reshape(-1)
+    rows = rows[rows >= 0]
+    assert (host(a)[rows] == r["a"][rows]).all()
+    assert (host(sa)[rows].view(np.uint32) == r["a_scale"][rows].view(np.uint32)).all()
+    # the last chunk (possibly a single token) through the chunk loop equals a standalone call
+    c0 = (wl.M - 1) // chunk * chunk if chunk else 0
+    tail = dict(d, x=d["x"][c0:].contiguous(), ids=d["ids"][c0:].contiguous(), w=d["w"][c0:].contiguous())
+    assert (gpu_forward(tail, wl.E, chunk=chunk) == got[c0:]).all()
+
+
+@pytest.mark.slow
+def test_qwen3_prefill_full_size():
+    check_full_size(mi.make_layer_inputs(mi.QWEN3_PREFILL), None, 24)
+
+
+@pytest.mark.slow
+def test_qwen3_chunked_local_full_size():
+    check_full_size(mi.make_layer_inputs(mi.QWEN3_CHUNKED), 128, 24)

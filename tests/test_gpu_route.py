@@ -1,0 +1,177 @@
+"""GPU parity of count / scatter / gather / SiLU-mul-quant against the CPU oracle,
+called through the C ABI. Integer and quantised outputs are compared bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_count_gb300 as moe
+import moe_inputs as mi
+import oracle
+from helpers import dev, host, host_bits, e4m3_ulp_diff
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def routing(M, topk, E, local, seed, zipf=0.0):
+    ids, w = mi.route(M, E, topk, seed=seed, zipf_s=zipf)
+    if local == "random":
+        m, El = mi.random_expert_map(E, max(1, E // 3), seed=seed), max(1, E // 3)
+    elif local == "none_local":
+        m, El = np.full(E, -1, np.int32), 4
+    elif local is None:
+        m, El = None, E
+    else:
+        m, El = mi.expert_map(E, local), local
+    return ids, w, m, El
+
+
+SWEEP = [(M, topk, E, local)
+         for M in (1, 2, 127, 128, 129, 1000)
+         for topk, E in ((1, 1), (2, 8), (8, 128))
+         for local in (None, "half", "random")
+         if not (E == 1 and local is not None)]
+
+
+def _local(E, local):
+    return E // 2 if local == "half" else local
+
+
+@pytest.mark.parametrize("M,topk,E,local", SWEEP + [(5000, 8, 128, None), (70000, 8, 128, "half"),
+                                                   (300, 8, 128, "none_local"), (0, 8, 128, None)])
+def test_count_bit_exact(M, topk, E, local):
+    ids, _, m, El = routing(M, topk, E, _local(E, local), seed=M + topk)
+    ref, bad = oracle.count(ids, E, El, m)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = moe.moe_count_expert_tokens(dev(ids), E, El, None if m is None else dev(m), err_count=err)
+    assert (host(got) == ref).all()
+    assert int(err.item()) == bad == 0
+
+
+def test_count_bad_ids():
+    ids = np.array([[0, -1], [5, 1], [-7, 1], [3, 3]], np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = moe.moe_count_expert_tokens(dev(ids), 4, 4, err_count=err)
+    ref, bad = oracle.count(ids, 4, 4)
+    assert (host(got) == ref).all() and int(err.item()) == bad == 2
+
+
+def run_scatter(x, ids, w, E, El, m, apply_on_input=False, quant=True):
+    xd, idsd, wd = dev(x), dev(ids), dev(w)
+    md = None if m is None else dev(m)
+    counts = moe.moe_count_expert_tokens(idsd, E, El, md)
+    q = moe.MOE_QUANT_FP8_1X128 if quant else moe.MOE_QUANT_NONE
+    a, sa, offs, s2d = moe.moe_scatter(xd, idsd, wd, E, El, counts, md, apply_on_input, q)
+    torch.cuda.synchronize()
+    return a, sa, host(offs), host(s2d), host(counts)
+
+
+def compare_scatter(x, ids, w, E, El, m, apply_on_input=False, quant=True):
+    a, sa, offs, s2d, counts = run_scatter(x, ids, w, E, El, m, apply_on_input, quant)
+    r = oracle.scatter(x, ids, w, E, El, m, apply_router_weight_on_input=apply_on_input, quant=quant)
+    assert (counts == r["counts"]).all()
+    assert (offs == r["offsets"]).all()
+    assert (s2d == r["src2dst"]).all()
+    rows = s2d.reshape(-1)
+    rows = rows[rows >= 0]
+    if quant:
+        assert (host(a)[rows] == r["a"][rows]).all(), "fp8 codes differ"
+        assert (host(sa)[rows].view(np.uint32) == r["a_scale"][rows].view(np.uint32)).all(), "scales differ"
+    else:
+        assert (host_bits(a)[rows] == r["a"][rows]).all()
+    return r
+
+
+@pytest.mark.parametrize("M,topk,E,local", SWEEP[::2] + [(5000, 8, 128, None), (300, 8, 128, "none_local")])
+def test_scatter_bit_exact(M, topk, E, local):
+    K = 256 if M < 1000 else 384
+    ids, w, m, El = routing(M, topk, E, _local(E, local), seed=3 * M + topk, zipf=1.2)
+    x = mi.hidden_states(M, K, seed=M)
+    compare_scatter(x, ids, w, E, El, m)
+
+
+@pytest.mark.parametrize("quant", [True, False])
+@pytest.mark.parametrize("apply_on_input", [False, True])
+def test_scatter_variants(quant, apply_on_input):
+    M, topk, E, K = 333, 4, 16, 640
+    ids, w, m, El = routing(M, topk, E, 10, seed=9)
+    x = mi.hidden_states(M, K, seed=9)
+    x[5, :128] = 0          # an all-zero group: scale 0, codes 0
+    x[6, 128:256] = x[6, 128]  # a constant group
+    compare_scatter(x, ids, w, E, El, m, apply_on_input, quant)
+
+
+def test_scatter_special_values():
+    """Rows with subnormal-range values, exact midpoints and saturating amax."""
+    K, E = 256, 2
+    rows = np.zeros((4, K), np.float32)
+    rows[0] = np.linspace(-1e-6, 1e-6, K)
+    rows[1, :] = 448.0
+    rows[1, ::3] = -224.0
+    rows[2] = np.tile(np.array([1.0, 1.0625, 1.1875, 17.0], np.float32), K // 4)  # scale 17/448
+    rows[3] = np.random.default_rng(1).standard_normal(K).astype(np.float32) * 1e4
+    x = mi.bf16_bits(rows)
+    ids = np.array([[0], [1], [0], [1]], np.int32)
+    w = np.ones((4, 1), np.float32)
+    compare_scatter(x, ids, w, E, E, None)
+
+
+def test_permute_only_workload_roundtrip():
+    """The permute/unpermute-only workload (experts = identity): bf16 copy then gather
+    returns x exactly; with FP8 the codes/scales/indices match the oracle bit for bit
+    and gather(bf16(dequant(A))) matches the oracle's gather bit for bit."""
+    wl = mi.PERMUTE_ONLY
+    li = mi.make_layer_inputs(wl)
+    a, _, _, s2d, _ = run_scatter(li.x, li.topk_ids, li.topk_weights, wl.E, wl.E, None, quant=False)
+    out = moe.moe_gather_weight_reduce(a, dev(s2d), dev(li.topk_weights))
+    torch.cuda.synchronize()
+    assert (mi.bf16_to_f32(host_bits(out)) == mi.bf16_to_f32(li.x)).all()
+    r = compare_scatter(li.x, li.topk_ids, li.topk_weights, wl.E, wl.E, None)
+    deq = torch.from_numpy(r["a"]).view(torch.float8_e4m3fn).float().numpy() * np.repeat(r["a_scale"], 128, 1)
+    Y = mi.bf16_bits(deq)
+    out = moe.moe_gather_weight_reduce(dev(Y), dev(r["src2dst"]), dev(li.topk_weights))
+    torch.cuda.synchronize()
+    ref = oracle.gather(Y, r["src2dst"], li.topk_weights)
+    assert (host_bits(out) == ref).all()
+
+
+@pytest.mark.parametrize("M,topk,K,drop", [(1, 1, 128, False), (129, 2, 384, True), (1000, 8, 2048, True),
+                                           (77, 32, 256, True)])
+@pytest.mark.parametrize("apply_on_input", [False, True])
+def test_gather_bit_exact(M, topk, K, drop, apply_on_input):
+    rng = np.random.default_rng(M)
+    R = M * topk + 5
+    Y = mi.bf16_bits(rng.standard_normal((R, K)).astype(np.float32))
+    s2d = rng.permutation(R)[: M * topk].reshape(M, topk).astype(np.int32)
+    if drop:
+        s2d[rng.random(s2d.shape) < 0.2] = -1
+        s2d[0, :] = -1
+    w = rng.random((M, topk)).astype(np.float32)
+    out = moe.moe_gather_weight_reduce(dev(Y), dev(s2d), dev(w), apply_on_input)
+    torch.cuda.synchronize()
+    ref = oracle.gather(Y, s2d, w, apply_on_input)
+    assert (host_bits(out) == ref).all()
+
+
+@pytest.mark.parametrize("N,counts", [(128, [3, 0, 130]), (768, [1, 64, 5, 0, 200])])
+def test_silu_mul_quant(N, counts):
+    rng = np.random.default_rng(N)
+    counts = np.array(counts, np.int32)
+    offs = oracle.offsets(counts)
+    R = int(offs[-1])
+    c1 = (rng.standard_normal((R, 2 * N)) * rng.uniform(0.01, 20, (R, 1))).astype(np.float32)
+    c1[0, :N] = 0.0
+    h, hs = moe.moe_silu_mul_quant(dev(c1), dev(offs))
+    torch.cuda.synchronize()
+    Href, hsref = oracle.silu_mul_quant(c1, offs, counts)
+    rows = np.concatenate([np.arange(offs[l], offs[l] + counts[l]) for l in range(len(counts))])
+    gh, ghs = host(h)[rows], host(hs)[rows]
+    # fp32 SiLU on the GPU vs fp64 in the oracle: scales within a few ulp, codes within 1 step
+    np.testing.assert_allclose(ghs, hsref[rows], rtol=4e-7, atol=0)
+    d = e4m3_ulp_diff(gh, Href[rows])
+    assert d.max() <= 1 and (d == 0).mean() >= 0.999
