@@ -1,0 +1,519 @@
+"""Benchmark of the fused-MoE layer hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one MoE-layer forward (count -> scatter + FP8 quant -> grouped FP8 GEMM w13
+with SiLU-and-mul requant -> grouped FP8 GEMM w2 -> gather + top-k weight-and-reduce,
+under the chunking loop) over one batch of seeded synthetic tokens already resident in
+HBM. Default workload: the Qwen3-30B-A3B-shaped layer at prefill size (M=8192 tokens,
+hidden 2048, moe intermediate 768, 128 experts, top-8, Zipf-skewed routing).
+
+Prints ONE JSON line (rank 0). With N > 1 (torchrun, one process per GPU) every rank
+runs its own batch (weak scaling, no data-path collective); the time is the max over
+ranks. `--impl reference` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs as mi  # noqa: E402
+
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "moe_expert_layer_count_gb300", "csrc")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=mi.QWEN3_PREFILL.name, choices=sorted(mi.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, src="fallback")
+
+
+# ------------------------------------------------------------------ algorithmic work
+def algorithmic(li, counts_per_chunk):
+    """Algorithmic bytes / flops per step (valid rows only; padding, re-reads and
+    weight re-streams beyond one per chunk are not credited)."""
+    wl = li.wl
+    M, K, N, topk = wl.M, wl.K, wl.N, wl.topk
+    R = int(sum(int(c.sum()) for c in counts_per_chunk))
+    n_slots = M * topk
+    a = {}
+    a["count_bytes"] = n_slots * 4 + (wl.E * 4 if wl.local_experts else 0)
+    a["scatter_bytes"] = M * K * 2 + R * K + R * (K // 128) * 4 + n_slots * 4 * 2
+    a["gather_bytes"] = R * K * 2 + M * K * 2 + n_slots * 8
+    if N:
+        a["gemm1_flops"] = 2.0 * R * (2 * N) * K
+        a["gemm2_flops"] = 2.0 * R * K * N
+        touched = sum(int((c > 0).sum()) for c in counts_per_chunk)
+        a["weight_bytes"] = touched * (3 * N * K + (2 * N // 128) * (K // 128) * 4 + (K // 128) * (N // 128) * 4)
+    a["R"] = R
+    return a
+
+
+def src_hash(fname):
+    with open(os.path.join(CSRC, fname), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch for `kernel` on `workload` from the committed ncu summary,
+    or None when absent or taken on a different version of the kernel's source."""
+    path = os.path.join(PROFILES, "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[workload][kernel]
+        if rec["src_sha"] != src_hash(rec["src"]):
+            return None
+        return float(rec["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# -------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [r for t, r in self.rows if self.t_on and self.t_on <= t <= (self.t_off or t)]
+        if not rows:
+            rows = [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import moe_expert_layer_count_gb300 as moe
+    moe.lib()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = mi.WORKLOADS[args.workload]
+    li = mi.make_layer_inputs(wl)
+    E, El, M, K, N, topk = wl.E, wl.El, wl.M, wl.K, wl.N, wl.topk
+    chunk = wl.chunk
+
+    def D(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    x, ids, tw = D(li.x), D(li.topk_ids), D(li.topk_weights)
+    emap = None if li.expert_map is None else D(li.expert_map)
+    permute_only = N == 0
+    stream = torch.cuda.current_stream()
+    cmax = min(chunk, M)
+    out = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    if not permute_only:
+        w13, s13, w2, s2 = D(li.w13), D(li.w13_scale), D(li.w2), D(li.w2_scale)
+        ws = torch.empty(moe.moe_workspace_size(cmax, K, N, topk, El), dtype=torch.uint8, device=dev)
+
+        def step():
+            moe.moe_forward_chunked(x, ids, tw, w13, s13, w2, s2, E, expert_map=emap, chunk_size=chunk,
+                                    out=out, workspace=ws)
+    else:
+        cap = moe.moe_rp_cap(M, topk, El)
+        A = torch.empty(cap, K, dtype=torch.uint8, device=dev)
+        SA = torch.empty(cap, K // 128, dtype=torch.float32, device=dev)
+        offs = torch.empty(El + 1, dtype=torch.int32, device=dev)
+        s2d = torch.empty(M, topk, dtype=torch.int32, device=dev)
+        cnt = torch.empty(El, dtype=torch.int32, device=dev)
+        sws = torch.empty(moe.moe_scatter_workspace_size(M, topk, El), dtype=torch.uint8, device=dev)
+        # identity experts: Y is the bf16 permuted copy of x
+        Y, _, _, _ = moe.moe_scatter(x, ids, tw, E, El, moe.moe_count_expert_tokens(ids, E, El, emap), emap,
+                                     quant=moe.MOE_QUANT_NONE)
+
+        def step():
+            moe.moe_count_expert_tokens(ids, E, El, emap, expert_num_tokens=cnt)
+            moe.moe_scatter(x, ids, tw, E, El, cnt, emap, rp_cap=cap, a_out=A, a_scale=SA, expert_offsets=offs,
+                            src2dst=s2d, workspace=sws)
+            moe.moe_gather_weight_reduce(Y, s2d, tw, out=out)
+
+    # per-chunk counts (host side, for the algorithmic work only)
+    counts = []
+    for c0 in range(0, M, chunk):
+        c = torch.zeros(El, dtype=torch.int32, device=dev)
+        moe.moe_count_expert_tokens(ids[c0:c0 + chunk].contiguous(), E, El, emap, expert_num_tokens=c)
+        counts.append(c.cpu().numpy())
+    work = algorithmic(li, counts)
+
+    clk = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
+                       if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
+    clk.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    l0 = moe.moe_kernel_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk.mark_on()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk.mark_off()
+    launches = (moe.moe_kernel_launch_count() - l0)
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        dist.barrier()
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clk.stop()
+
+    # ---- per-kernel breakdown on the same stream (separate loop, same calls) ----
+    kern = kernel_breakdown(moe, torch, stream, li, x, ids, tw, emap, dev, args, permute_only,
+                            locals().get("w13"), locals().get("s13"), locals().get("w2"), locals().get("s2"))
+
+    # ---- end to end: pinned host inputs -> device -> layer -> host output, per step ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(moe, torch, stream, li, dev, args, step, x, ids, tw, out)
+
+    tokens = M * world
+    value = tokens / (ms / 1e3)
+    pk = peaks()
+    roof = roofline(kern, work, pk, wl)
+    line = {
+        "metric": "MoE-layer tokens/s",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3" if not permute_only else "bf16/fp8_e4m3",
+        "data": "synthetic: seeded N(0,1) bf16 tokens, N(0,1)+Zipf router logits, random-init N(0,0.02) "
+                "weights quantised to FP8 e4m3 with 128x128 block scales",
+        "config": {"workload": wl.name, "M": M, "hidden": K, "moe_intermediate": N, "experts": E,
+                   "local_experts": El, "topk": topk, "chunk_size": chunk,
+                   "routing": f"zipf s={wl.zipf_s}" if wl.zipf_s else "uniform",
+                   "parallelism": f"replicas x{world} (one independent batch per GPU)",
+                   "l2": "inputs larger than L2 (expert weights %.0f MB + activations)" %
+                         (work.get("weight_bytes", 0) / 1e6) if not permute_only else
+                         "inputs larger than L2 (x %.0f MB + permuted rows %.0f MB)" %
+                         (M * K * 2 / 1e6, work["R"] * K * 3 / 1e6)},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "roofline": roof,
+        "kernels": kern["table"],
+        "scatter_gbs": kern["table"].get("scatter", {}).get("GB/s"),
+        "gather_gbs": kern["table"].get("gather", {}).get("GB/s"),
+        "gemm_tflops": kern["table"].get("gemm1", {}).get("TFLOP/s"),
+        "e2e": e2e,
+    }
+    return line
+
+
+def kernel_breakdown(moe, torch, stream, li, x, ids, tw, emap, dev, args, permute_only, w13, s13, w2, s2):
+    """Time each stage of one chunk-loop pass with CUDA events on the launching stream,
+    calling the same entry points the layer's chunk loop calls."""
+    wl = li.wl
+    E, El, M, K, N, topk, chunk = wl.E, wl.El, wl.M, wl.K, wl.N, wl.topk, wl.chunk
+    cmax = min(chunk, M)
+    cap = moe.moe_rp_cap(cmax, topk, El)
+    cnt = torch.empty(El, dtype=torch.int32, device=dev)
+    A = torch.empty(cap, K, dtype=torch.uint8, device=dev)
+    SA = torch.empty(cap, K // 128, dtype=torch.float32, device=dev)
+    offs = torch.empty(El + 1, dtype=torch.int32, device=dev)
+    s2d = torch.empty(cmax, topk, dtype=torch.int32, device=dev)
+    sws = torch.empty(moe.moe_scatter_workspace_size(cmax, topk, El), dtype=torch.uint8, device=dev)
+    Y = torch.empty(cap, K, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    if not permute_only:
+        H = torch.empty(cap, N, dtype=torch.uint8, device=dev)
+        HS = torch.empty(cap, N // 128, dtype=torch.float32, device=dev)
+        fused = FUSED_SILU
+        C1 = None if fused else torch.empty(cap, 2 * N, dtype=torch.float32, device=dev)
+    stages = ["count", "scatter"] + ([] if permute_only else (["gemm1"] + ([] if FUSED_SILU else ["silu"]) +
+                                                               ["gemm2"])) + ["gather"]
+    reps = max(3, min(args.steps, 20))
+    times = {s: 0.0 for s in stages}
+    launches = {s: 0 for s in stages}
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    for it in range(reps + 2):
+        for c0 in range(0, M, chunk):
+            Mc = min(chunk, M - c0)
+            capc = moe.moe_rp_cap(Mc, topk, El)
+            e = [ev() for _ in range(len(stages) + 1)]
+            xi, ii, wi = x[c0:c0 + Mc], ids[c0:c0 + Mc], tw[c0:c0 + Mc]
+            n0 = moe.moe_kernel_launch_count()
+            marks = []
+            e[0].record(stream)
+            j = 0
+            moe.moe_count_expert_tokens(ii, E, El, emap, expert_num_tokens=cnt); marks.append(moe.moe_kernel_launch_count())
+            e[1].record(stream)
+            moe.moe_scatter(xi, ii, wi, E, El, cnt, emap, rp_cap=capc, a_out=A[:capc], a_scale=SA[:capc],
+                            expert_offsets=offs, src2dst=s2d[:Mc], workspace=sws)
+            marks.append(moe.moe_kernel_launch_count())
+            e[2].record(stream)
+            j = 2
+            if permute_only:
+                Yv = Y[:capc]
+            else:
+                if FUSED_SILU:
+                    moe.moe_grouped_gemm_fp8(A[:capc], SA[:capc], w13, s13, offs, moe.MOE_EPI_SILU_MUL_QUANT,
+                                             out=H[:capc], out_scale=HS[:capc])
+                    marks.append(moe.moe_kernel_launch_count())
+                    j += 1
+                    e[j].record(stream)
+                else:
+                    moe.moe_grouped_gemm_fp8(A[:capc], SA[:capc], w13, s13, offs, moe.MOE_EPI_F32, out=C1[:capc])
+                    marks.append(moe.moe_kernel_launch_count())
+                    j += 1
+                    e[j].record(stream)
+                    moe.moe_silu_mul_quant(C1[:capc], offs, h=H[:capc], h_scale=HS[:capc])
+                    marks.append(moe.moe_kernel_launch_count())
+                    j += 1
+                    e[j].record(stream)
+                moe.moe_grouped_gemm_fp8(H[:capc], HS[:capc], w2, s2, offs, moe.MOE_EPI_BF16, out=Y[:capc])
+                marks.append(moe.moe_kernel_launch_count())
+                j += 1
+                e[j].record(stream)
+                Yv = Y[:capc]
+            moe.moe_gather_weight_reduce(Yv, s2d[:Mc], wi, out=out[c0:c0 + Mc])
+            marks.append(moe.moe_kernel_launch_count())
+            j += 1
+            e[j].record(stream)
+            torch.cuda.synchronize()
+            if it >= 2:
+                prev = n0
+                for si, s in enumerate(stages):
+                    times[s] += e[si].elapsed_time(e[si + 1])
+                    launches[s] += marks[si] - prev
+                    prev = marks[si]
+    table = {}
+    for s in stages:
+        us = times[s] / reps * 1e3
+        table[s] = {"us_per_step": round(us, 2), "launches_per_step": launches[s] // reps}
+    return {"table": table}
+
+
+def roofline(kern, work, pk, wl):
+    t = kern["table"]
+    for s, key in (("count", "count_bytes"), ("scatter", "scatter_bytes"), ("gather", "gather_bytes")):
+        if s in t and t[s]["us_per_step"] > 0:
+            t[s]["GB/s"] = round(work[key] / (t[s]["us_per_step"] * 1e-6) / 1e9, 1)
+            t[s]["hbm_frac"] = round(t[s]["GB/s"] / pk["hbm"], 4)
+    fp8_peak = 2.0 * pk["bf16"]   # dense FP8 = 2x dense bf16 (nominal ratio 4.5 / 2.25 PFLOP/s)
+    for s, key in (("gemm1", "gemm1_flops"), ("gemm2", "gemm2_flops")):
+        if s in t and t[s]["us_per_step"] > 0:
+            t[s]["TFLOP/s"] = round(work[key] / (t[s]["us_per_step"] * 1e-6) / 1e12, 1)
+            t[s]["tensor_frac"] = round(t[s]["TFLOP/s"] / fp8_peak, 4)
+    dom = max(t, key=lambda s: t[s]["us_per_step"])
+    launches = max(1, t[dom]["launches_per_step"])
+    if dom.startswith("gemm"):
+        achieved = t[dom]["TFLOP/s"]
+        traffic = recorded_traffic(dom, wl.name)
+        return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                "peak_source": f"{pk['src']} bf16 {pk['bf16']} TFLOP/s x 2 (dense fp8/bf16 nominal ratio)",
+                "traffic": None if traffic is None else traffic,
+                "algorithmic_per_launch": work[dom + "_flops"] / launches}
+    achieved = t[dom].get("GB/s")
+    traffic = recorded_traffic(dom, wl.name)
+    return {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm"], 4) if achieved else None,
+            "peak_source": f"{pk['src']} copy bandwidth", "traffic": traffic,
+            "algorithmic_per_launch": work[dom + "_bytes"] / launches}
+
+
+FUSED_SILU = True  # GEMM1 applies SiLU-and-mul + FP8 requant in its epilogue (as the chunk loop does)
+
+
+def end_to_end(moe, torch, stream, li, dev, args, step_dev, x, ids, tw, out):
+    """Same metric through the public API with host buffers: every step copies that
+    step's inputs from pinned host memory to the device and reads the output back."""
+    wl = li.wl
+    xh = torch.from_numpy(np.ascontiguousarray(li.x).view(np.int16)).view(torch.bfloat16).pin_memory()
+    ih = torch.from_numpy(np.ascontiguousarray(li.topk_ids)).pin_memory()
+    wh = torch.from_numpy(np.ascontiguousarray(li.topk_weights)).pin_memory()
+    oh = torch.empty(wl.M, wl.K, dtype=torch.bfloat16).pin_memory()
+
+    def step():
+        x.copy_(xh, non_blocking=True)
+        ids.copy_(ih, non_blocking=True)
+        tw.copy_(wh, non_blocking=True)
+        step_dev()
+        oh.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(wl.M / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(xh.numel() * 2 + ih.numel() * 4 + wh.numel() * 4),
+            "d2h_bytes_per_step": int(oh.numel() * 2), "steps": steps}
+
+
+# ------------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, target_s=12.0):
+    """Times the CPU oracle (as it stands, single-threaded C) on a bounded sample of the
+    workload: its first m tokens, m grown until one call takes ~target_s."""
+    import oracle
+    li = mi.make_layer_inputs(wl)
+    m = 4
+    while True:
+        t0 = time.perf_counter()
+        if wl.N:
+            oracle.forward_chunked(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], li.w13, li.w13_scale, li.w2,
+                                   li.w2_scale, wl.E, expert_map=li.expert_map, chunk_size=wl.chunk)
+        else:
+            r = oracle.scatter(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], wl.E, wl.El, li.expert_map)
+            oracle.gather(mi.bf16_bits(np.zeros((r["a"].shape[0], wl.K), np.float32)), r["src2dst"],
+                          li.topk_weights[:m])
+        dt = time.perf_counter() - t0
+        if dt >= target_s or m >= wl.M:
+            return li, m, dt
+        m = min(wl.M, max(m * 2, int(m * target_s / max(dt, 1e-3) * 1.1)))
+
+
+def cpu_baseline(wl):
+    _, m, dt = oracle_sample(wl)
+    return {"value": round(m / dt, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {m} of {wl.M} tokens of {wl.name} (single-threaded C oracle, {dt:.1f} s)"}
+
+
+def run_reference(args):
+    wl = mi.WORKLOADS[args.workload]
+    li, m, _ = oracle_sample(wl, target_s=4.0)
+    import oracle
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        if wl.N:
+            oracle.forward_chunked(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], li.w13, li.w13_scale, li.w2,
+                                   li.w2_scale, wl.E, expert_map=li.expert_map, chunk_size=wl.chunk)
+        else:
+            r = oracle.scatter(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], wl.E, wl.El, li.expert_map)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    s = sum(times)
+    value = m * len(times) / s
+    return {"impl": "reference", "metric": "MoE-layer tokens/s", "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(s / len(times) * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp64 (oracle)", "data": "synthetic",
+            "config": {"workload": wl.name, "M": wl.M, "sample_tokens_per_step": m},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"first {m} of {wl.M} tokens per step"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(mi.WORKLOADS[args.workload])
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

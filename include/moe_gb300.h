@@ -81,6 +81,12 @@ MOE_API const char* moe_status_string(int status);
  * streams), for accounting in benchmarks. */
 MOE_API uint64_t moe_kernel_launch_count(void);
 
+/* Device-side error word of this library's kernels on the current device: 0 when no
+ * kernel has reported a problem, 1 when a grouped-GEMM pipeline wait gave up after its
+ * time limit (the kernel then returned early and its output is not valid). Reading it
+ * synchronises the device; clear != 0 resets it to 0. Returns -1 if the read failed. */
+MOE_API int moe_device_error(int clear);
+
 /* Row bound of the permuted buffers for a chunk of chunk_M tokens:
  * roundup128(chunk_M*topk + min(local_num_experts, chunk_M*topk) * 127). Every
  * non-empty expert pads its block by at most 127 rows, so expert_offsets[El] never

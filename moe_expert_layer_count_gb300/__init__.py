@@ -53,6 +53,7 @@ _p, _i64, _int, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_si
 SIGNATURES = {
     "moe_status_string": ([_int], ctypes.c_char_p),
     "moe_kernel_launch_count": ([], ctypes.c_uint64),
+    "moe_device_error": ([_int], _int),
     "moe_rp_cap": ([_i64, _int, _int], _i64),
     "moe_scatter_workspace_size": ([_i64, _int, _int], _sz),
     "moe_workspace_size": ([_i64, _int, _int, _int, _int], _sz),
@@ -105,6 +106,11 @@ def status_string(status: int) -> str:
 
 def moe_kernel_launch_count() -> int:
     return int(lib().moe_kernel_launch_count())
+
+
+def moe_device_error(clear: bool = False) -> int:
+    """The library's device error word (0 = fine); synchronises the device."""
+    return int(lib().moe_device_error(int(bool(clear))))
 
 
 def moe_rp_cap(chunk_M: int, topk: int, local_num_experts: int) -> int:

@@ -47,9 +47,9 @@ bool routing_args_ok(int64_t M, int topk, int E, int El) {
 //   counts  int32 [El]        offsets int32 [El+1]     src2dst int32 [Mc*topk]
 //   hist    scatter scratch   region1 = A e4m3 [cap,K] + A_scale fp32 [cap,K/128], later
 //                                       reused by Y bf16 [cap,K] (A is dead after GEMM1)
-//   C1      fp32 [cap, 2N]    H e4m3 [cap, N]          H_scale fp32 [cap, N/128]
+//   H       e4m3 [cap, N]     H_scale fp32 [cap, N/128]  (written by GEMM1's SiLU epilogue)
 struct Carve {
-    size_t counts, offsets, src2dst, hist, a, a_scale, y, c1, h, h_scale, total;
+    size_t counts, offsets, src2dst, hist, a, a_scale, y, h, h_scale, total;
 };
 
 Carve carve(int64_t Mc, int K, int N, int topk, int El) {
@@ -66,7 +66,6 @@ Carve carve(int64_t Mc, int K, int N, int topk, int El) {
     c.a_scale = p + align256((size_t)cap * K);
     c.y = p;
     p += a_bytes > y_bytes ? a_bytes : y_bytes;
-    c.c1 = p;       p += align256((size_t)cap * 2 * N * 4);
     c.h = p;        p += align256((size_t)cap * N);
     c.h_scale = p;  p += align256((size_t)cap * (N / kGroup) * 4);
     c.total = p;
@@ -92,6 +91,8 @@ MOE_API const char* moe_status_string(int status) {
 }
 
 MOE_API uint64_t moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+MOE_API int moe_device_error(int clear) { return read_gemm_error(clear); }
 
 MOE_API int64_t moe_rp_cap(int64_t chunk_M, int topk, int local_num_experts) {
     if (chunk_M < 0 || topk < 1 || local_num_experts < 1) return -1;
@@ -231,7 +232,6 @@ MOE_API int moe_forward_chunked(const void* hidden_states, const int32_t* topk_i
         uint8_t* A = ws + cv.a;
         float* sa = reinterpret_cast<float*>(ws + cv.a_scale);
         uint16_t* Y = reinterpret_cast<uint16_t*>(ws + cv.y);
-        float* c1 = reinterpret_cast<float*>(ws + cv.c1);
         uint8_t* H = ws + cv.h;
         float* sh = reinterpret_cast<float*>(ws + cv.h_scale);
         const int32_t* ids = topk_ids + c0 * topk;
@@ -240,8 +240,9 @@ MOE_API int moe_forward_chunked(const void* hidden_states, const int32_t* topk_i
         if (!st)
             st = launch_scatter(x + c0 * K, Mc, K, ids, tw, topk, expert_map, E, El, counts,
                                 apply_router_weight_on_input ? 1 : 0, MOE_QUANT_FP8_1X128, A, sa, offs, s2d, hist, s);
-        if (!st) st = launch_grouped_gemm(A, sa, w13, w13_scale, offs, El, cap, 2 * N, K, MOE_EPI_F32, c1, nullptr, sms, s);
-        if (!st) st = launch_silu_mul_quant(c1, offs, El, cap, N, H, sh, s);
+        if (!st)
+            st = launch_grouped_gemm(A, sa, w13, w13_scale, offs, El, cap, 2 * N, K, MOE_EPI_SILU_MUL_QUANT, H, sh,
+                                     sms, s);
         if (!st) st = launch_grouped_gemm(H, sh, w2, w2_scale, offs, El, cap, K, N, MOE_EPI_BF16, Y, nullptr, sms, s);
         if (!st) st = launch_gather(Y, s2d, tw, Mc, topk, K, apply_router_weight_on_input ? 1 : 0, o + c0 * K, s);
         if (st) return st;

@@ -1,0 +1,410 @@
+// Block-scaled FP8 grouped GEMM on the 5th-generation tensor cores (tcgen05, sm_103a):
+//   out[r, j] = sum_kb a_scale[r, kb] * w_scale[l, j/128, kb] * sum_{k in kb} A[r,k] W[l,j,k]
+// for the rows r of every local expert l's 128-aligned block -- the DeepGEMM "m-grouped
+// contiguous" GEMM of vLLM PR #20903 "[Kernel] DeepGemm MoE : Integrate triton permute
+// / unpermute kernels", section "Optimizations" (float8_e4m3fn, --block-shape 128 128).
+//
+// Design (one persistent CTA per SM, warp-specialised):
+//  * warp 8 (one thread) streams 128x128 A tiles and BNx128 W tiles into a ring of
+//    shared-memory stages with TMA (128-byte swizzle), one stage per 128-wide K block;
+//  * warp 9 (one thread) issues tcgen05.mma kind::f8f6f4 (M=128, N=BN, K=32, four per
+//    K block) into one of two TMEM accumulators, starting each K block from zero;
+//  * warps 0-7 (two warpgroups, each one TMEM lane = one row per thread, half of the
+//    tile's columns each) read the K block's partial sums from TMEM, release the buffer
+//    and fold them into fp32 registers with the product of the two block scales. The
+//    scales are fp32 amax/448 values, not powers of two, so they are applied here in
+//    software rather than by the block-scaled MMA kinds. Double-buffering TMEM lets the
+//    MMA of block kb+1 run while block kb is promoted.
+//  * Epilogues: bf16 or fp32 rows, or SiLU-and-mul with 1x128 FP8 requantisation. For
+//    the latter the W tile is gate rows [j, j+64) | up rows [j, j+64) | gate [j+64, j+128)
+//    | up [j+64, j+128), so each warpgroup holds matching gate/up columns of 64 outputs
+//    and one amax exchange per row completes the 128-wide group.
+// Every wait on a pipeline barrier gives up after 2 s, sets a device error word and an
+// abort flag seen by all roles, waits (bounded) for its own copies and MMAs in flight,
+// and the CTA frees its TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "route.cuh"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+
+__device__ int g_gemm_error;  // set to 1 when a pipeline wait ran out of time
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 128;  // one K block: 128 fp8 = one 128-byte swizzled row
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = (kEpiWarps + 2) * 32;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kBoxRows = 64;  // W is loaded in 64-row TMA boxes
+
+template <int BN>
+struct Cfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kABytes = kBM * kBK;
+    static constexpr int kBBytes = BN * kBK;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kCols = BN / 2;  // accumulator columns per epilogue thread
+};
+
+struct __align__(8) Tail {
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t amax_bar[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int BN>
+constexpr size_t smem_bytes(int El) {
+    return 1024 + (size_t)Cfg<BN>::kStages * Cfg<BN>::kStageBytes + sizeof(Tail) + 2 * 2 * 128 * sizeof(float) +
+           (size_t)(El + 1) * sizeof(int32_t);
+}
+
+// Bounded wait on an mbarrier phase. With check_abort, returns false as soon as another
+// role has aborted; otherwise waits for the phase or the time limit only.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort, bool check_abort = true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 31) == 0) {
+            if (check_abort && *abort) return false;
+            if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
+                *abort = 1;
+                atomicExch(&g_gemm_error, 1);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ int expert_of(const int32_t* s_off, int El, int row0) {
+    int lo = 0, hi = El - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= row0) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fmul_rn(__fdiv_rn(g, 1.0f + expf(-g)), u); }
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const float* __restrict__ sa, const float* __restrict__ sw, const int32_t* __restrict__ offsets,
+                   int El, int n_out, int k_in, void* __restrict__ out, float* __restrict__ out_scale) {
+    using C = Cfg<BN>;
+    constexpr bool kSilu = EPI == MOE_EPI_SILU_MUL_QUANT;
+    static_assert(!kSilu || BN == 256, "the SiLU epilogue pairs 128 gate with 128 up columns");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Tail* st = reinterpret_cast<Tail*>(smem + C::kStages * C::kStageBytes);
+    float* s_amax = reinterpret_cast<float*>(st + 1);  // [2 parities][2 warpgroups][128 rows]
+    int32_t* s_off = reinterpret_cast<int32_t*>(s_amax + 2 * 2 * 128);
+    volatile int* abort = &st->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i <= El; i += kThreads) s_off[i] = __ldg(offsets + i);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&st->full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&st->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_addr(&st->tfull[b]), 1);
+            ptx::mbar_init(ptx::smem_addr(&st->tempty[b]), kEpiWarps);
+            ptx::mbar_init(ptx::smem_addr(&st->amax_bar[b]), kEpiWarps * 32);
+        }
+        ptx::mbar_init(ptx::smem_addr(&st->mma_done), 1);
+        st->abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(&st->tmem_base), C::kTmemCols);
+        ptx::tmem_relinquish();
+        ptx::tc_fence_before();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+    }
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = st->tmem_base;
+
+    const int m_tiles = s_off[El] / kBM;
+    const int n_tiles = kSilu ? n_out / 256 : n_out / BN;
+    const int tiles = m_tiles * n_tiles;
+    const int KB = k_in / kBK;
+    const int NB = n_out / 128;  // weight-scale blocks along n_out
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+                const int mt = tile / n_tiles, nt = tile % n_tiles;
+                const int row0 = mt * kBM;
+                const int l = expert_of(s_off, El, row0);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    const uint32_t ph = (it / C::kStages) & 1;
+                    if (!wait_phase(ptx::smem_addr(&st->empty[s]), ph ^ 1, abort)) { ok = false; break; }
+                    const uint32_t full = ptx::smem_addr(&st->full[s]);
+                    ptx::mbar_arrive_expect_tx(full, C::kStageBytes);
+                    const uint32_t a_dst = ptx::smem_addr(smem + s * C::kStageBytes);
+                    const uint32_t b_dst = a_dst + C::kABytes;
+                    ptx::tma_load_2d(a_dst, &tmA, kb * kBK, row0, full);
+#pragma unroll
+                    for (int p = 0; p < BN / kBoxRows; ++p) {
+                        int brow;
+                        if (kSilu)  // gate | up | gate | up, 64 rows each
+                            brow = l * n_out + (p & 1) * (n_out / 2) + nt * 128 + (p >> 1) * kBoxRows;
+                        else
+                            brow = l * n_out + nt * BN + p * kBoxRows;
+                        ptx::tma_load_2d(b_dst + p * kBoxRows * kBK, &tmB, kb * kBK, brow, full);
+                    }
+                }
+            }
+            // never leave with copies in flight: the last stages' loads must have landed
+            const uint32_t first = it > (uint32_t)C::kStages ? it - C::kStages : 0;
+            for (uint32_t j = first; j < it; ++j)
+                wait_phase(ptx::smem_addr(&st->full[j % C::kStages]), (j / C::kStages) & 1, abort, false);
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kBM, BN);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    const uint32_t ph = (it / C::kStages) & 1;
+                    const int b = it & 1;
+                    const uint32_t tph = (it >> 1) & 1;
+                    if (!wait_phase(ptx::smem_addr(&st->tempty[b]), tph ^ 1, abort)) { ok = false; break; }
+                    if (!wait_phase(ptx::smem_addr(&st->full[s]), ph, abort)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t a_base = ptx::smem_addr(smem + s * C::kStageBytes);
+                    const uint32_t b_base = a_base + C::kABytes;
+                    const uint32_t d = tmem + (uint32_t)(b * BN);
+#pragma unroll
+                    for (int k = 0; k < kBK / 32; ++k)
+                        ptx::mma_f8f6f4(d, ptx::smem_desc_sw128(a_base + 32 * k, 1024),
+                                        ptx::smem_desc_sw128(b_base + 32 * k, 1024), idesc, k > 0 ? 1u : 0u);
+                    ptx::mma_commit(ptx::smem_addr(&st->empty[s]));
+                    ptx::mma_commit(ptx::smem_addr(&st->tfull[b]));
+                }
+            }
+            // never leave with MMAs in flight
+            ptx::mma_commit(ptx::smem_addr(&st->mma_done));
+            wait_phase(ptx::smem_addr(&st->mma_done), 0, abort, false);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int wg = warp >> 2;
+        const int row_in_tile = (warp & 3) * 32 + lane;
+        const uint32_t lane_field = (uint32_t)((warp & 3) * 32) << 16;
+        uint32_t it = 0;
+        int tcount = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++tcount) {
+            const int mt = tile / n_tiles, nt = tile % n_tiles;
+            const int row0 = mt * kBM;
+            const int l = expert_of(s_off, El, row0);
+            const int64_t r = row0 + row_in_tile;
+            float acc[C::kCols];
+#pragma unroll
+            for (int c = 0; c < C::kCols; ++c) acc[c] = 0.f;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int b = it & 1;
+                const uint32_t tph = (it >> 1) & 1;
+                bool got = wait_phase(ptx::smem_addr(&st->tfull[b]), tph, abort);
+                got = __all_sync(0xffffffffu, got);
+                if (!got) { ok = false; break; }
+                ptx::tc_fence_after();
+                const float sr = __ldg(sa + r * KB + kb);
+                float s0, s1;
+                if (kSilu) {
+                    s0 = sr * __ldg(sw + ((int64_t)l * NB + nt) * KB + kb);               // gate block
+                    s1 = sr * __ldg(sw + ((int64_t)l * NB + NB / 2 + nt) * KB + kb);      // up block
+                } else {
+                    const int nb = BN == 256 ? nt * 2 + wg : nt;
+                    s0 = s1 = sr * __ldg(sw + ((int64_t)l * NB + nb) * KB + kb);
+                }
+                const uint32_t tbase = tmem + lane_field + (uint32_t)(b * BN + wg * C::kCols);
+#pragma unroll
+                for (int c = 0; c < C::kCols; c += 32) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(tbase + c, v);
+                    ptx::tmem_wait_ld();
+                    const float s = (c < C::kCols / 2) ? s0 : s1;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[c + i] = fmaf(s, __uint_as_float(v[i]), acc[c + i]);
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&st->tempty[b]));
+            }
+            if (!ok) break;
+            if (kSilu) {
+                // acc[0:64) gate, acc[64:128) up of h columns nt*128 + wg*64 + [0, 64)
+                const int N = n_out / 2;
+                float amax = 0.f;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    acc[j] = silu_mul(acc[j], acc[64 + j]);
+                    amax = fmaxf(amax, fabsf(acc[j]));
+                }
+                float* xa = s_amax + (tcount & 1) * 256;
+                xa[wg * 128 + row_in_tile] = amax;
+                const uint32_t abar = ptx::smem_addr(&st->amax_bar[tcount & 1]);
+                ptx::mbar_arrive(abar);
+                bool got = wait_phase(abar, (tcount >> 1) & 1, abort);
+                got = __all_sync(0xffffffffu, got);
+                if (!got) { ok = false; break; }
+                amax = fmaxf(xa[row_in_tile], xa[128 + row_in_tile]);
+                const float s = __fdiv_rn(amax, 448.0f);
+                uint32_t w[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    uint16_t lo = 0, hi = 0;
+                    if (s != 0.f) {
+                        lo = f32x2_to_e4m3x2(__fdiv_rn(acc[4 * q + 0], s), __fdiv_rn(acc[4 * q + 1], s));
+                        hi = f32x2_to_e4m3x2(__fdiv_rn(acc[4 * q + 2], s), __fdiv_rn(acc[4 * q + 3], s));
+                    }
+                    w[q] = uint32_t(lo) | (uint32_t(hi) << 16);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + r * N + nt * 128 + wg * 64);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                if (wg == 0) out_scale[r * (N / 128) + nt] = s;
+            } else if (EPI == MOE_EPI_F32) {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + r * n_out + nt * BN + wg * C::kCols);
+#pragma unroll
+                for (int q = 0; q < C::kCols / 4; ++q)
+                    dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+            } else {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + r * n_out + nt * BN + wg * C::kCols);
+#pragma unroll
+                for (int q = 0; q < C::kCols / 8; ++q) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = uint32_t(f32_to_bf16_bits(acc[8 * q + 2 * e])) |
+                               (uint32_t(f32_to_bf16_bits(acc[8 * q + 2 * e + 1])) << 16);
+                    dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D uint8 tensor [rows, inner] (row-major), boxes of box_rows x 128 bytes, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* w_scale,
+              const int32_t* offsets, int El, int64_t rp_cap, int n_out, int k_in, void* out, float* out_scale,
+              int num_sms, cudaStream_t stream) {
+    const size_t smem = smem_bytes<BN>(El);
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem_bytes<BN>(kMaxLocalExperts));
+    });
+    if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+    const int n_tiles = EPI == MOE_EPI_SILU_MUL_QUANT ? n_out / 256 : n_out / BN;
+    const int64_t max_tiles = rp_cap / kBM * n_tiles;
+    const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
+    if (grid < 1) return MOE_OK;
+    gemm_tc_kernel<BN, EPI><<<grid, kThreads, smem, stream>>>(ta, tb, a_scale, w_scale, offsets, El, n_out, k_in, out,
+                                                             out_scale);
+    note_launches(1);
+    return launch_status();
+}
+
+}  // namespace
+
+int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
+                        const int32_t* expert_offsets, int El, int64_t rp_cap, int n_out, int k_in, int epilogue,
+                        void* out, float* out_scale, int num_sms, cudaStream_t stream) {
+    if (rp_cap == 0) return MOE_OK;
+    const bool bn256 = n_out % 256 == 0;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, a, (uint64_t)k_in, (uint64_t)rp_cap, kBM) ||
+        !make_tmap(&tb, w, (uint64_t)k_in, (uint64_t)El * n_out, kBoxRows))
+        return MOE_ERR_CUDA;
+    switch (epilogue) {
+        case MOE_EPI_SILU_MUL_QUANT:
+            return launch_tc<256, MOE_EPI_SILU_MUL_QUANT>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+                                                          k_in, out, out_scale, num_sms, stream);
+        case MOE_EPI_F32:
+            return bn256 ? launch_tc<256, MOE_EPI_F32>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+                                                       k_in, out, out_scale, num_sms, stream)
+                         : launch_tc<128, MOE_EPI_F32>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+                                                       k_in, out, out_scale, num_sms, stream);
+        default:
+            return bn256 ? launch_tc<256, MOE_EPI_BF16>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+                                                        k_in, out, out_scale, num_sms, stream)
+                         : launch_tc<128, MOE_EPI_BF16>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+                                                        k_in, out, out_scale, num_sms, stream);
+    }
+}
+
+int read_gemm_error(int clear) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(int)) != cudaSuccess) return -1;
+    if (clear && v) {
+        const int z = 0;
+        cudaMemcpyToSymbol(g_gemm_error, &z, sizeof(int));
+    }
+    return v;
+}
+
+}  // namespace moe

@@ -31,4 +31,8 @@ int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w
                         const int32_t* expert_offsets, int El, int64_t rp_cap, int n_out, int k_in, int epilogue,
                         void* out, float* out_scale, int num_sms, cudaStream_t stream);
 
+// Device error word of the grouped GEMM (1: a pipeline wait ran out of time). Reading
+// it synchronises the device; `clear` resets it.
+int read_gemm_error(int clear);
+
 }  // namespace moe

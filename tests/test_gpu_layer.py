@@ -55,6 +55,32 @@ def test_grouped_gemm_matches_oracle(counts, n_out, k_in, epi):
     assert err.max() <= tol * np.abs(ref).max(), err.max() / np.abs(ref).max()
 
 
+@pytest.mark.parametrize("counts,N,K", [([5, 0, 130], 256, 384), ([1, 300, 17, 0, 64], 768, 2048)])
+def test_grouped_gemm_silu_epilogue(counts, N, K):
+    """GEMM1 with the fused SiLU-and-mul + FP8 requant epilogue: equal, bit for bit, to the
+    fp32-output GEMM followed by the standalone SiLU-mul-quant kernel, and within one e4m3
+    step of the oracle (fp64 GEMM, fp64 SiLU)."""
+    counts, offs, A, SA = permuted_inputs(counts, K, seed=N)
+    El = len(counts)
+    W, S = mi.expert_weights(El, 2 * N, K, seed=11, stream=1)
+    h, hs = moe.moe_grouped_gemm_fp8(dev(A), dev(SA), dev(W), dev(S), dev(offs), moe.MOE_EPI_SILU_MUL_QUANT)
+    c1 = moe.moe_grouped_gemm_fp8(dev(A), dev(SA), dev(W), dev(S), dev(offs), moe.MOE_EPI_F32)
+    h2, hs2 = moe.moe_silu_mul_quant(c1, dev(offs))
+    torch.cuda.synchronize()
+    rows = kept_rows(offs, counts)
+    assert (host(h)[rows] == host(h2)[rows]).all()
+    assert (host(hs)[rows].view(np.uint32) == host(hs2)[rows].view(np.uint32)).all()
+    C1 = oracle.grouped_gemm(A, SA, W, S, offs, counts).astype(np.float32)
+    Href, hsref = oracle.silu_mul_quant(C1, offs, counts)
+    np.testing.assert_allclose(host(hs)[rows], hsref[rows], rtol=2e-5, atol=0)
+    d = e4m3_ulp_diff(host(h)[rows], Href[rows])
+    assert d.max() <= 1 and (d == 0).mean() >= 0.99
+
+
+def test_device_error_word_is_clear():
+    assert moe.moe_device_error() == 0
+
+
 def test_grouped_gemm_identity_weights_bit_exact():
     """W = block-diagonal 1.0, scale 1: each output is a single product, no summation
     order freedom, so the fp32 results equal the oracle's exactly."""
