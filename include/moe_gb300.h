@@ -60,6 +60,7 @@ enum moe_status {
     MOE_ERR_WORKSPACE_TOO_SMALL = 2, /* workspace_bytes below the size query's answer */
     MOE_ERR_UNSUPPORTED_DEVICE = 3,  /* the current device is not compute capability 10.3 */
     MOE_ERR_CUDA = 4,                /* a CUDA call or launch failed */
+    MOE_ERR_SCRATCH_LIMIT = 5,       /* moe_scatter_noalloc: problem too large for its fixed scratch */
 };
 
 enum moe_quant {
@@ -134,6 +135,30 @@ MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32
                         int local_num_experts, const int32_t* expert_num_tokens, int apply_router_weight_on_input,
                         int quant, void* a_out, float* a_scale, int32_t* expert_offsets, int32_t* src2dst,
                         int64_t rp_cap, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_scatter without a workspace argument, for callers that cannot allocate device
+ * memory: for example an inference engine that plans every device buffer once at
+ * start-up and allows no allocation on its request path (cudaMalloc may synchronise the
+ * device and may fail when memory is fragmented), or a host runtime that only passes
+ * input and output buffers. The vLLM pages have no counterpart: this is an interface
+ * convenience of this library, not a step of the method.
+ * Arguments and results are those of moe_scatter (minus workspace/workspace_bytes).
+ * The scratch it needs (per-block expert histograms) is a fixed array of 65536 int32
+ * (256 KiB) in this library's own device memory, held by every GPU that loads the
+ * library until the process exits. A problem needing more -- (number of scatter blocks)
+ * x local_num_experts > 65536 when more than one block is used, e.g. beyond about
+ * 131k top-k slots at 1024 local experts or about 16.7M slots at 128 -- is refused with
+ * MOE_ERR_SCRATCH_LIMIT before anything is enqueued.
+ * The first call on each device looks up the array's device address (with that device
+ * current); make that first call before any stream capture. Every call on a device
+ * shares the one array and overwrites the entries it reads, so calls whose kernels
+ * overlap on the GPU (different streams, no ordering between them) race and give wrong
+ * results: order them on one stream or with events. Allocates nothing. */
+MOE_API int moe_scatter_noalloc(const void* hidden_states, int64_t M, int K, const int32_t* topk_ids,
+                                const float* topk_weights, int topk, const int32_t* expert_map, int E,
+                                int local_num_experts, const int32_t* expert_num_tokens,
+                                int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
+                                int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, moe_stream_t stream);
 
 /* The DeepGEMM-style grouped ("m-grouped contiguous") GEMM with 128x128 block-scaled
  * FP8 weights ([P1] Optimizations, --block-shape 128 128), on tcgen05 tensor cores:

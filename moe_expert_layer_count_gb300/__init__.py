@@ -60,6 +60,8 @@ SIGNATURES = {
     "moe_count_expert_tokens": ([_p, _i64, _int, _p, _int, _int, _p, _p, _p], _int),
     "moe_scatter": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _int, _p, _p, _p, _p, _i64,
                      _p, _sz, _p], _int),
+    "moe_scatter_noalloc": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _int, _p, _p, _p, _p, _i64,
+                             _p], _int),
     "moe_grouped_gemm_fp8": ([_p, _p, _p, _p, _p, _int, _i64, _int, _int, _int, _p, _p, _p], _int),
     "moe_silu_mul_quant": ([_p, _p, _int, _i64, _int, _p, _p, _p], _int),
     "moe_gather_weight_reduce": ([_p, _p, _p, _i64, _int, _int, _int, _p, _p], _int),
@@ -168,6 +170,24 @@ def moe_scatter(hidden_states, topk_ids, topk_weights, E, local_num_experts, exp
         _ptr(hidden_states), M, K, _ptr(topk_ids), _ptr(topk_weights), topk, _ptr(expert_map), E, El,
         _ptr(expert_num_tokens), int(bool(apply_router_weight_on_input)), quant, _ptr(a_out), _ptr(a_scale),
         _ptr(expert_offsets), _ptr(src2dst), cap, _ptr(workspace), workspace.numel(), _stream(stream)))
+    return a_out, a_scale, expert_offsets, src2dst
+
+
+def moe_scatter_noalloc(hidden_states, topk_ids, topk_weights, E, local_num_experts, expert_num_tokens,
+                        a_out, a_scale, expert_offsets, src2dst, expert_map=None,
+                        apply_router_weight_on_input=False, quant=MOE_QUANT_FP8_1X128, rp_cap=None, stream=None):
+    """moe_scatter for callers that cannot allocate: every output buffer is the caller's,
+    and the scratch is a fixed array inside the library (see the C header for its limit
+    and for the rule that calls must not overlap on the GPU). Returns the outputs."""
+    _dt(hidden_states, torch.bfloat16, "hidden_states")
+    _dt(topk_ids, torch.int32, "topk_ids")
+    M, K = hidden_states.shape
+    topk = topk_ids.shape[1]
+    cap = a_out.shape[0] if rp_cap is None else rp_cap
+    _check("moe_scatter_noalloc", lib().moe_scatter_noalloc(
+        _ptr(hidden_states), M, K, _ptr(topk_ids), _ptr(topk_weights), topk, _ptr(expert_map), E,
+        local_num_experts, _ptr(expert_num_tokens), int(bool(apply_router_weight_on_input)), quant,
+        _ptr(a_out), _ptr(a_scale), _ptr(expert_offsets), _ptr(src2dst), cap, _stream(stream)))
     return a_out, a_scale, expert_offsets, src2dst
 
 

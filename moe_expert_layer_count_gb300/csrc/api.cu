@@ -86,6 +86,7 @@ MOE_API const char* moe_status_string(int status) {
         case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
         case MOE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3, sm_103a)";
         case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_SCRATCH_LIMIT: return "problem too large for the fixed scratch of moe_scatter_noalloc";
         default: return "unknown status";
     }
 }
