@@ -148,8 +148,9 @@ MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32
     if (multi && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if (int st = check_device(nullptr)) return st;
     return launch_scatter(static_cast<const uint16_t*>(hidden_states), M, K, topk_ids, topk_weights, topk, expert_map, E,
-                          local_num_experts, expert_num_tokens, apply_router_weight_on_input ? 1 : 0, quant, a_out,
-                          a_scale, expert_offsets, src2dst, static_cast<int32_t*>(workspace), (cudaStream_t)stream);
+                          local_num_experts, expert_num_tokens, nullptr, nullptr, apply_router_weight_on_input ? 1 : 0,
+                          quant, a_out, a_scale, expert_offsets, src2dst, static_cast<int32_t*>(workspace),
+                          (cudaStream_t)stream);
 }
 
 MOE_API int moe_grouped_gemm_fp8(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
@@ -237,9 +238,8 @@ MOE_API int moe_forward_chunked(const void* hidden_states, const int32_t* topk_i
         float* sh = reinterpret_cast<float*>(ws + cv.h_scale);
         const int32_t* ids = topk_ids + c0 * topk;
         const float* tw = topk_weights + c0 * topk;
-        int st = launch_count(ids, Mc * topk, expert_map, E, El, counts, err_count, sms, s);
-        if (!st)
-            st = launch_scatter(x + c0 * K, Mc, K, ids, tw, topk, expert_map, E, El, counts,
+        // the chunk's expert counts come out of the scatter's own histogram pass
+        int st = launch_scatter(x + c0 * K, Mc, K, ids, tw, topk, expert_map, E, El, nullptr, counts, err_count,
                                 apply_router_weight_on_input ? 1 : 0, MOE_QUANT_FP8_1X128, A, sa, offs, s2d, hist, s);
         if (!st)
             st = launch_grouped_gemm(A, sa, w13, w13_scale, offs, El, cap, 2 * N, K, MOE_EPI_SILU_MUL_QUANT, H, sh,

@@ -52,6 +52,24 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
+// SiLU-and-mul of the w13 GEMM's gate g and up u: silu(g) * u with silu(g) = g/(1+e^-g),
+// in fast fp32 (ex2.approx-based exponential, approximate division; a few ulp). The
+// exponent is clamped so that 1 + e^-g stays finite. The fused GEMM epilogue and the
+// standalone kernel both use this function, so their results are identical.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f))) * u;
+}
+
+// Correctly rounded quotient a / b (round-to-nearest-even) from r = RN(1/b): the
+// product a*r is within an ulp of the quotient, and one fused correction with the exact
+// remainder a - b*q gives RN(a/b) (Markstein's theorem for FMA division). Valid while
+// 1/b does not overflow; callers keep b in the normal range.
+__device__ __forceinline__ float div_rn_by(float a, float b, float r) {
+    const float q = __fmul_rn(a, r);
+    const float e = __fmaf_rn(-q, b, a);
+    return __fmaf_rn(e, r, q);
+}
+
 // Quantise 16 consecutive fp32 values of one 1x128 group (8 lanes x 16 values, the 8
 // lanes aligned on a multiple of 8 within the warp) to e4m3 with the group's fp32 scale
 // amax/448. Returns the 16 codes packed in a uint4 and the scale.

@@ -99,7 +99,6 @@ __device__ __forceinline__ int expert_of(const int32_t* s_off, int El, int row0)
     return lo;
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return __fmul_rn(__fdiv_rn(g, 1.0f + expf(-g)), u); }
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -226,40 +225,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row0 = mt * kBM;
             const int l = expert_of(s_off, El, row0);
             const int64_t r = row0 + row_in_tile;
-            float acc[C::kCols];
+            // fp32 accumulators as pairs, updated with packed fp32 FMAs (two per
+            // instruction, each rounded exactly like fmaf)
+            float2 acc2[C::kCols / 2];
 #pragma unroll
-            for (int c = 0; c < C::kCols; ++c) acc[c] = 0.f;
+            for (int c = 0; c < C::kCols / 2; ++c) acc2[c] = make_float2(0.f, 0.f);
+            // block scales of this tile, fetched one K block ahead of their use
+            const float* sa_row = sa + r * KB;
+            const float* sw0 = sw + ((int64_t)l * NB + (kSilu ? nt : (BN == 256 ? nt * 2 + wg : nt))) * KB;
+            const float* sw1 = kSilu ? sw + ((int64_t)l * NB + NB / 2 + nt) * KB : sw0;
+            float sr_n = __ldg(sa_row), s0_n = __ldg(sw0), s1_n = kSilu ? __ldg(sw1) : s0_n;
+            const uint32_t tcol = lane_field + (uint32_t)(wg * C::kCols);
             for (int kb = 0; kb < KB; ++kb, ++it) {
+                const float sr = sr_n, sb0 = s0_n, sb1 = s1_n;
+                if (kb + 1 < KB) {
+                    sr_n = __ldg(sa_row + kb + 1);
+                    s0_n = __ldg(sw0 + kb + 1);
+                    if (kSilu) s1_n = __ldg(sw1 + kb + 1);
+                }
                 const int b = it & 1;
                 const uint32_t tph = (it >> 1) & 1;
                 bool got = wait_phase(ptx::smem_addr(&st->tfull[b]), tph, abort);
                 got = __all_sync(0xffffffffu, got);
                 if (!got) { ok = false; break; }
                 ptx::tc_fence_after();
-                const float sr = __ldg(sa + r * KB + kb);
-                float s0, s1;
-                if (kSilu) {
-                    s0 = sr * __ldg(sw + ((int64_t)l * NB + nt) * KB + kb);               // gate block
-                    s1 = sr * __ldg(sw + ((int64_t)l * NB + NB / 2 + nt) * KB + kb);      // up block
-                } else {
-                    const int nb = BN == 256 ? nt * 2 + wg : nt;
-                    s0 = s1 = sr * __ldg(sw + ((int64_t)l * NB + nb) * KB + kb);
-                }
-                const uint32_t tbase = tmem + lane_field + (uint32_t)(b * BN + wg * C::kCols);
+                const float s0 = sr * sb0, s1 = kSilu ? sr * sb1 : s0;
+                const uint32_t tbase = tmem + tcol + (uint32_t)(b * BN);
+                // 16-column TMEM loads, double-buffered: the load of the next 16 columns
+                // is in flight while the current 16 are folded in
+                uint32_t va[16], vb[16];
+                ptx::tmem_ld_32x32b_x16(tbase, va);
 #pragma unroll
                 for (int c = 0; c < C::kCols; c += 32) {
-                    uint32_t v[32];
-                    ptx::tmem_ld_32x32b_x32(tbase + c, v);
-                    ptx::tmem_wait_ld();
-                    const float s = (c < C::kCols / 2) ? s0 : s1;
+                    ptx::tmem_wait_ld_regs(va);
+                    ptx::tmem_ld_32x32b_x16(tbase + c + 16, vb);
+                    const float sa_ = (c < C::kCols / 2) ? s0 : s1;
+                    const float2 sa2 = make_float2(sa_, sa_);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c + i] = fmaf(s, __uint_as_float(v[i]), acc[c + i]);
+                    for (int i = 0; i < 8; ++i)
+                        acc2[c / 2 + i] = __ffma2_rn(
+                            sa2, make_float2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1])),
+                            acc2[c / 2 + i]);
+                    ptx::tmem_wait_ld_regs(vb);
+                    if (c + 32 < C::kCols) ptx::tmem_ld_32x32b_x16(tbase + c + 32, va);
+                    const float sb_ = (c + 16 < C::kCols / 2) ? s0 : s1;
+                    const float2 sb2 = make_float2(sb_, sb_);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc2[c / 2 + 8 + i] = __ffma2_rn(
+                            sb2, make_float2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1])),
+                            acc2[c / 2 + 8 + i]);
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&st->tempty[b]));
             }
             if (!ok) break;
+            float* acc = reinterpret_cast<float*>(acc2);
             if (kSilu) {
                 // acc[0:64) gate, acc[64:128) up of h columns nt*128 + wg*64 + [0, 64)
                 const int N = n_out / 2;
@@ -278,15 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!got) { ok = false; break; }
                 amax = fmaxf(xa[row_in_tile], xa[128 + row_in_tile]);
                 const float s = __fdiv_rn(amax, 448.0f);
+                // code = e4m3(h / s) with the correctly rounded quotient
+                const bool fast = s >= 1e-30f;
+                const float rs = fast ? __frcp_rn(s) : 0.f;
                 uint32_t w[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
-                    uint16_t lo = 0, hi = 0;
-                    if (s != 0.f) {
-                        lo = f32x2_to_e4m3x2(__fdiv_rn(acc[4 * q + 0], s), __fdiv_rn(acc[4 * q + 1], s));
-                        hi = f32x2_to_e4m3x2(__fdiv_rn(acc[4 * q + 2], s), __fdiv_rn(acc[4 * q + 3], s));
-                    }
-                    w[q] = uint32_t(lo) | (uint32_t(hi) << 16);
+                    float d[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        d[j] = s == 0.f ? 0.f : (fast ? div_rn_by(acc[4 * q + j], s, rs) : __fdiv_rn(acc[4 * q + j], s));
+                    w[q] = uint32_t(f32x2_to_e4m3x2(d[0], d[1])) | (uint32_t(f32x2_to_e4m3x2(d[2], d[3])) << 16);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + r * N + nt * 128 + wg * 64);
 #pragma unroll

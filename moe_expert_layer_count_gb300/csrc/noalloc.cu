@@ -77,6 +77,7 @@ extern "C" MOE_API int moe_scatter_noalloc(const void* hidden_states, int64_t M,
     // the histogram kernel overwrites every entry the rank kernel then reads, so the
     // previous call's contents never leak into this one
     return launch_scatter(static_cast<const uint16_t*>(hidden_states), M, K, topk_ids, topk_weights, topk, expert_map,
-                          E, local_num_experts, expert_num_tokens, apply_router_weight_on_input ? 1 : 0, quant, a_out,
-                          a_scale, expert_offsets, src2dst, scratch, (cudaStream_t)stream);
+                          E, local_num_experts, expert_num_tokens, nullptr, nullptr,
+                          apply_router_weight_on_input ? 1 : 0, quant, a_out, a_scale, expert_offsets, src2dst, scratch,
+                          (cudaStream_t)stream);
 }

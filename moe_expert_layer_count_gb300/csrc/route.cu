@@ -14,18 +14,18 @@ namespace moe {
 
 // ------------------------------------------------------------------------ count
 // One CTA builds a shared-memory histogram of its share of the top-k slots (16-byte
-// id loads, warp-aggregated with __match_any_sync so that a popular expert costs one
-// shared atomic per warp), then stores it (single CTA) or adds it to the zeroed
-// global counts (one global atomic per CTA and expert).
+// id loads, four per thread issued back to back, warp-aggregated with __match_any_sync
+// so that a popular expert costs one shared atomic per warp), then stores it (single
+// CTA) or adds it to the zeroed global counts (one global atomic per CTA and expert).
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads)
     count_kernel(const int32_t* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E, int El,
                  int32_t* __restrict__ counts, int32_t* __restrict__ err_count, int direct) {
+    constexpr int kVec = 4;  // int4 loads in flight per thread
     extern __shared__ int32_t hist[];
     for (int l = threadIdx.x; l < El; l += kThreads) hist[l] = 0;
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
     int bad = 0;
     auto add = [&](int l) {
         const unsigned m = __match_any_sync(0xffffffffu, l);
@@ -34,16 +34,24 @@ __global__ void __launch_bounds__(kThreads)
     const bool vec = (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
     const int64_t n4 = vec ? n / 4 : 0;
     const int4* ids4 = reinterpret_cast<const int4*>(ids);
-    for (int64_t i0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); i0 < n4; i0 += stride) {
-        const int64_t i = i0 + lane;
-        int4 v = make_int4(-1, -1, -1, -1);
-        if (i < n4) v = __ldg(ids4 + i);
-        add(local_expert(v.x, expert_map, E, El, bad));
-        add(local_expert(v.y, expert_map, E, El, bad));
-        add(local_expert(v.z, expert_map, E, El, bad));
-        add(local_expert(v.w, expert_map, E, El, bad));
+    const int64_t step = (int64_t)gridDim.x * kThreads * kVec;
+    for (int64_t b0 = (int64_t)blockIdx.x * kThreads * kVec + (threadIdx.x & ~31) * kVec; b0 < n4; b0 += step) {
+        int4 v[kVec];
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const int64_t i = b0 + j * 32 + lane;
+            v[j] = i < n4 ? __ldg(ids4 + i) : make_int4(-1, -1, -1, -1);
+        }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            add(local_expert(v[j].x, expert_map, E, El, bad));
+            add(local_expert(v[j].y, expert_map, E, El, bad));
+            add(local_expert(v[j].z, expert_map, E, El, bad));
+            add(local_expert(v[j].w, expert_map, E, El, bad));
+        }
     }
-    for (int64_t i0 = 4 * n4 + (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); i0 < n; i0 += stride) {
+    for (int64_t i0 = 4 * n4 + (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); i0 < n;
+         i0 += (int64_t)gridDim.x * kThreads) {
         const int64_t i = i0 + lane;
         add(i < n ? local_expert(__ldg(ids + i), expert_map, E, El, bad) : -1);
     }
@@ -64,18 +72,17 @@ __global__ void __launch_bounds__(kThreads)
 
 int launch_count(const int32_t* ids, int64_t n, const int32_t* expert_map, int E, int El, int32_t* counts,
                  int32_t* err_count, int num_sms, cudaStream_t stream) {
-    constexpr int kThreads = 1024;
     const size_t smem = (size_t)El * sizeof(int32_t);
-    if (n <= 32768) {
-        count_kernel<kThreads><<<1, kThreads, smem, stream>>>(ids, n, expert_map, E, El, counts, err_count, 1);
+    if (n <= 16384) {  // one CTA, one batch of loads per thread: no memset needed
+        count_kernel<1024><<<1, 1024, smem, stream>>>(ids, n, expert_map, E, El, counts, err_count, 1);
         note_launches(1);
         return launch_status();
     }
+    // 256-thread CTAs, 4096 slots each (one batch of 16 ids per thread), adding into zeros
     if (cudaMemsetAsync(counts, 0, (size_t)El * sizeof(int32_t), stream) != cudaSuccess) return MOE_ERR_CUDA;
-    int64_t want = (n / 4 + kThreads - 1) / kThreads;
-    int grid = (int)(want < 2 * num_sms ? want : 2 * num_sms);
-    if (grid < 1) grid = 1;
-    count_kernel<kThreads><<<grid, kThreads, smem, stream>>>(ids, n, expert_map, E, El, counts, err_count, 0);
+    const int64_t want = (n + 4095) / 4096;
+    const int grid = (int)(want < 4 * num_sms ? want : 4 * num_sms);
+    count_kernel<256><<<grid, 256, smem, stream>>>(ids, n, expert_map, E, El, counts, err_count, 0);
     note_launches(1);
     return launch_status();
 }
@@ -83,52 +90,160 @@ int launch_count(const int32_t* ids, int64_t n, const int32_t* expert_map, int E
 // ---------------------------------------------------------------------- scatter
 // The stable permutation is a counting sort over the flat slot index i = t*topk + k:
 //   dst(i) = offsets[l] + #{ i' < i : local(i') == l }.
-// The slots are cut into contiguous per-CTA segments. Kernel 1 writes each segment's
-// expert histogram; kernel 2 adds the histograms of the earlier segments to the
-// expert offsets and ranks its own slots warp by warp (warp segments in order, 32
-// slots at a time, rank within the 32 by __match_any_sync + popc). Kernel 3 copies
-// and quantises the rows. Nothing depends on timing, so the order is unique.
+// The slots are cut into contiguous per-CTA segments, and each CTA's segment into 8
+// contiguous warp segments walked 256 slots at a time (8 groups of 32, loaded back to
+// back before any is used). Kernel 1 writes each segment's expert histogram; kernel 2
+// adds the histograms of the earlier segments to the expert offsets and ranks its own
+// slots (rank inside a group of 32 by __match_any_sync + popc, per-warp running
+// cursors in shared memory). Kernel 3 copies and quantises the rows. Nothing depends
+// on timing, so the order is unique.
+
+constexpr int kRound = 8;  // groups of 32 slots loaded per warp per round
 
 int scatter_slots_per_cta(int64_t n) {
+    constexpr int64_t kUnit = (kScatterThreads / 32) * 32 * kRound;  // 2048: one round for each warp
     int64_t per = (n + kMaxScatterCtas - 1) / kMaxScatterCtas;
-    per = (per + kScatterThreads - 1) / kScatterThreads * kScatterThreads;
+    per = (per + kUnit - 1) / kUnit * kUnit;
     return (int)(per < kScatterMinSlots ? kScatterMinSlots : per);
+}
+
+// Local experts of one round of a warp's segment: slot base + 32 j + lane, j < kRound.
+__device__ __forceinline__ void load_round(const int32_t* __restrict__ ids, int64_t base, int64_t end,
+                                           const int32_t* __restrict__ expert_map, int E, int El, int lane,
+                                           int (&l)[kRound], int& bad) {
+    int id[kRound];
+#pragma unroll
+    for (int j = 0; j < kRound; ++j) {
+        const int64_t i = base + j * 32 + lane;
+        id[j] = i < end ? __ldg(ids + i) : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kRound; ++j) l[j] = local_expert(id[j], expert_map, E, El, bad);
 }
 
 __global__ void __launch_bounds__(kScatterThreads)
     scatter_hist_kernel(const int32_t* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E,
-                        int El, int per_cta, int32_t* __restrict__ hist) {
+                        int El, int per_cta, int32_t* __restrict__ hist, int32_t* __restrict__ err_count) {
     extern __shared__ int32_t sh[];
     for (int l = threadIdx.x; l < El; l += kScatterThreads) sh[l] = 0;
     __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const int64_t begin = (int64_t)blockIdx.x * per_cta;
-    const int64_t end = min(n, begin + per_cta);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per_warp = per_cta / (kScatterThreads / 32);
+    const int64_t wbeg = (int64_t)blockIdx.x * per_cta + (int64_t)warp * per_warp;
+    const int64_t wend = min(n, wbeg + per_warp);
     int bad = 0;
-    for (int64_t i0 = begin + (threadIdx.x & ~31); i0 < end; i0 += kScatterThreads) {
-        const int64_t i = i0 + lane;
-        const int l = i < end ? local_expert(__ldg(ids + i), expert_map, E, El, bad) : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, l);
-        if (l >= 0 && lane == __ffs(m) - 1) atomicAdd(&sh[l], __popc(m));
+    for (int64_t r0 = wbeg; r0 < wend; r0 += 32 * kRound) {
+        int l[kRound];
+        load_round(ids, r0, wend, expert_map, E, El, lane, l, bad);
+#pragma unroll
+        for (int j = 0; j < kRound; ++j) {
+            const unsigned m = __match_any_sync(0xffffffffu, l[j]);
+            if (l[j] >= 0 && lane == __ffs(m) - 1) atomicAdd(&sh[l[j]], __popc(m));
+        }
+    }
+    if (err_count) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        if (lane == 0 && bad) atomicAdd(err_count, bad);
     }
     __syncthreads();
     for (int l = threadIdx.x; l < El; l += kScatterThreads) hist[(int64_t)blockIdx.x * El + l] = sh[l];
 }
 
+// counts_in: the experts' slot counts (moe_scatter's input). When it is NULL the counts
+// are derived here -- from all CTAs' histograms, or from this single CTA's own pass --
+// and written to counts_out (the chunk loop's count step, fused into the scatter).
 __global__ void __launch_bounds__(kScatterThreads)
     scatter_rank_kernel(const int32_t* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E,
-                        int El, int per_cta, const int32_t* __restrict__ counts, const int32_t* __restrict__ hist,
-                        int32_t* __restrict__ expert_offsets, int32_t* __restrict__ src2dst) {
+                        int El, int per_cta, const int32_t* __restrict__ counts_in, const int32_t* __restrict__ hist,
+                        int32_t* __restrict__ expert_offsets, int32_t* __restrict__ src2dst,
+                        int32_t* __restrict__ counts_out, int32_t* __restrict__ err_count) {
     constexpr int kWarps = kScatterThreads / 32;
     extern __shared__ int32_t sm[];
-    int32_t* off = sm;           // [El + 1]
-    int32_t* wc = sm + El + 1;   // [kWarps][El]: per-warp counts, then per-warp cursors
+    int32_t* off = sm;               // [El + 1]
+    int32_t* base = sm + El + 1;     // [El]: slots of the earlier CTAs
+    int32_t* tot = base + El;        // [El]: slots of all CTAs (counts derived here)
+    int32_t* wc = tot + El;          // [kWarps][El]: per-warp counts, then per-warp cursors
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (warp == 0) {
+    const int G = gridDim.x;
+    const int per_warp = per_cta / kWarps;
+    const int64_t wbeg = (int64_t)blockIdx.x * per_cta + (int64_t)warp * per_warp;
+    const int64_t wend = min(n, wbeg + per_warp);
+    int bad = 0;
+    // the first round of this warp's slots, in flight while the histograms are summed
+    int l0[kRound];
+    load_round(ids, wbeg, wend, expert_map, E, El, lane, l0, bad);
+    for (int l = threadIdx.x; l < El; l += kScatterThreads) base[l] = tot[l] = 0;
+    for (int i = threadIdx.x; i < kWarps * El; i += kScatterThreads) wc[i] = 0;
+    __syncthreads();
+    const bool derive = counts_in == nullptr;
+    if (G > 1) {
+        // per expert: sum of the earlier CTAs' histograms (and of all, when deriving the
+        // counts); several threads per expert, loads issued 8 at a time
+        const int rows = derive ? G : (int)blockIdx.x;
+        const int tpl = El >= kScatterThreads ? 1 : kScatterThreads / El;
+        for (int t = threadIdx.x; t < tpl * El; t += kScatterThreads) {
+            const int l = t % El, part = t / El;
+            int pre = 0, all = 0;
+            for (int b0 = part; b0 < rows; b0 += 8 * tpl) {
+                int v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int b = b0 + j * tpl;
+                    v[j] = b < rows ? __ldg(hist + (int64_t)b * El + l) : 0;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int b = b0 + j * tpl;
+                    all += v[j];
+                    if (b < (int)blockIdx.x) pre += v[j];
+                }
+            }
+            if (pre) atomicAdd(&base[l], pre);
+            if (all) atomicAdd(&tot[l], all);
+        }
+    }
+    int32_t* mine = wc + warp * El;
+    for (int64_t r0 = wbeg; r0 < wend; r0 += 32 * kRound) {
+        int l[kRound];
+        if (r0 == wbeg) {
+#pragma unroll
+            for (int j = 0; j < kRound; ++j) l[j] = l0[j];
+        } else {
+            load_round(ids, r0, wend, expert_map, E, El, lane, l, bad);
+        }
+#pragma unroll
+        for (int j = 0; j < kRound; ++j) {
+            const unsigned m = __match_any_sync(0xffffffffu, l[j]);
+            if (l[j] >= 0 && lane == __ffs(m) - 1) mine[l[j]] += __popc(m);
+            __syncwarp();
+        }
+    }
+    if (derive && G == 1 && err_count) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        if (lane == 0 && bad) atomicAdd(err_count, bad);
+    }
+    __syncthreads();
+    for (int l = threadIdx.x; l < El; l += kScatterThreads) {
+        int c;
+        if (!derive) {
+            c = __ldg(counts_in + l);
+        } else if (G > 1) {
+            c = tot[l];
+        } else {
+            c = 0;
+            for (int w = 0; w < kWarps; ++w) c += wc[w * El + l];
+        }
+        if (derive && blockIdx.x == 0) counts_out[l] = c;
+        off[l] = (c + kGroup - 1) / kGroup * kGroup;  // padded block sizes, scanned below
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive scan of the padded block sizes
         int run = 0;
-        for (int l0 = 0; l0 < El; l0 += 32) {
-            const int l = l0 + lane;
-            const int c = l < El ? (__ldg(counts + l) + kGroup - 1) / kGroup * kGroup : 0;
+        for (int lb = 0; lb < El; lb += 32) {
+            const int l = lb + lane;
+            const int c = l < El ? off[l] : 0;
             int incl = c;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -140,27 +255,11 @@ __global__ void __launch_bounds__(kScatterThreads)
         }
         if (lane == 0) off[El] = run;
     }
-    for (int i = threadIdx.x; i < kWarps * El; i += kScatterThreads) wc[i] = 0;
     __syncthreads();
     if (blockIdx.x == 0)
         for (int l = threadIdx.x; l <= El; l += kScatterThreads) expert_offsets[l] = off[l];
-
-    const int per_warp = per_cta / kWarps;
-    const int64_t wbeg = (int64_t)blockIdx.x * per_cta + (int64_t)warp * per_warp;
-    const int64_t wend = min(n, wbeg + per_warp);
-    int bad = 0;
-    int32_t* mine = wc + warp * El;
-    for (int64_t i0 = wbeg; i0 < wend; i0 += 32) {
-        const int64_t i = i0 + lane;
-        const int l = i < wend ? local_expert(__ldg(ids + i), expert_map, E, El, bad) : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, l);
-        if (l >= 0 && lane == __ffs(m) - 1) mine[l] += __popc(m);
-        __syncwarp();
-    }
-    __syncthreads();
     for (int l = threadIdx.x; l < El; l += kScatterThreads) {
-        int run = off[l];
-        for (int b = 0; b < (int)blockIdx.x; ++b) run += __ldg(hist + (int64_t)b * El + l);
+        int run = off[l] + base[l];
         for (int w = 0; w < kWarps; ++w) {
             const int c = wc[w * El + l];
             wc[w * El + l] = run;
@@ -168,21 +267,33 @@ __global__ void __launch_bounds__(kScatterThreads)
         }
     }
     __syncthreads();
-    for (int64_t i0 = wbeg; i0 < wend; i0 += 32) {
-        const int64_t i = i0 + lane;
-        const bool valid = i < wend;
-        const int l = valid ? local_expert(__ldg(ids + i), expert_map, E, El, bad) : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, l);
-        const int rank = __popc(m & lanemask_lt());
-        int dst = -1;
-        if (l >= 0) {
-            dst = mine[l] + rank;
-            if (dst >= off[l + 1]) dst = -1;  // counts inconsistent with ids: drop, never overflow
+    for (int64_t r0 = wbeg; r0 < wend; r0 += 32 * kRound) {
+        int l[kRound];
+        if (r0 == wbeg) {
+#pragma unroll
+            for (int j = 0; j < kRound; ++j) l[j] = l0[j];
+        } else {
+            load_round(ids, r0, wend, expert_map, E, El, lane, l, bad);
         }
-        __syncwarp();
-        if (l >= 0 && rank == 0) mine[l] += __popc(m);
-        __syncwarp();
-        if (valid) src2dst[i] = dst;
+        int dst[kRound];
+#pragma unroll
+        for (int j = 0; j < kRound; ++j) {
+            const unsigned m = __match_any_sync(0xffffffffu, l[j]);
+            const int rank = __popc(m & lanemask_lt());
+            dst[j] = -1;
+            if (l[j] >= 0) {
+                dst[j] = mine[l[j]] + rank;
+                if (dst[j] >= off[l[j] + 1]) dst[j] = -1;  // counts inconsistent with ids: drop, never overflow
+            }
+            __syncwarp();
+            if (l[j] >= 0 && rank == 0) mine[l[j]] += __popc(m);
+            __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < kRound; ++j) {
+            const int64_t i = r0 + j * 32 + lane;
+            if (i < wend) src2dst[i] = dst[j];
+        }
     }
 }
 
@@ -264,21 +375,22 @@ __global__ void __launch_bounds__(256)
 }
 
 int launch_scatter(const uint16_t* x, int64_t M, int K, const int32_t* ids, const float* topk_weights, int topk,
-                   const int32_t* expert_map, int E, int El, const int32_t* counts, int apply_on_input, int quant,
-                   void* a_out, float* a_scale, int32_t* expert_offsets, int32_t* src2dst, int32_t* hist,
-                   cudaStream_t stream) {
+                   const int32_t* expert_map, int E, int El, const int32_t* counts_in, int32_t* counts_out,
+                   int32_t* err_count, int apply_on_input, int quant, void* a_out, float* a_scale,
+                   int32_t* expert_offsets, int32_t* src2dst, int32_t* hist, cudaStream_t stream) {
     const int64_t n = M * topk;
     const int per_cta = scatter_slots_per_cta(n);
     const int grid = (int)((n + per_cta - 1) / per_cta);
-    const size_t smem_rank = (size_t)(El + 1 + (kScatterThreads / 32) * El) * sizeof(int32_t);
+    const size_t smem_rank = (size_t)(3 * El + 1 + (kScatterThreads / 32) * El) * sizeof(int32_t);
     int launches = 0;
     if (grid > 1) {
-        scatter_hist_kernel<<<grid, kScatterThreads, (size_t)El * sizeof(int32_t), stream>>>(ids, n, expert_map, E, El,
-                                                                                              per_cta, hist);
+        scatter_hist_kernel<<<grid, kScatterThreads, (size_t)El * sizeof(int32_t), stream>>>(
+            ids, n, expert_map, E, El, per_cta, hist, counts_in ? nullptr : err_count);
         ++launches;
     }
     scatter_rank_kernel<<<grid < 1 ? 1 : grid, kScatterThreads, smem_rank, stream>>>(
-        ids, n, expert_map, E, El, per_cta, counts, hist, expert_offsets, src2dst);
+        ids, n, expert_map, E, El, per_cta, counts_in, hist, expert_offsets, src2dst, counts_out,
+        counts_in ? nullptr : err_count);
     ++launches;
     if (M > 0) {
         const int64_t warps = M * ((K + 511) / 512);
@@ -356,7 +468,29 @@ int launch_gather(const uint16_t* y, const int32_t* src2dst, const float* topk_w
 }
 
 // ------------------------------------------------------------- SiLU-and-mul quant
-__device__ __forceinline__ float silu_mul(float g, float u) { return __fmul_rn(__fdiv_rn(g, 1.0f + expf(-g)), u); }
+// Requantisation of 16 h values of one 1x128 group (8 lanes x 16): scale = amax/448,
+// code = e4m3(h/scale) with the correctly rounded quotient (same rule as the scatter).
+__device__ __forceinline__ uint4 requant16_group8(const float (&v)[16], float& scale_out) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = __fdiv_rn(amax, 448.0f);
+    scale_out = s;
+    const bool fast = s >= 1e-30f;  // 1/s finite and normal
+    const float r = fast ? __frcp_rn(s) : 0.f;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            q[j] = s == 0.f ? 0.f : (fast ? div_rn_by(v[4 * i + j], s, r) : __fdiv_rn(v[4 * i + j], s));
+        w[i] = uint32_t(f32x2_to_e4m3x2(q[0], q[1])) | (uint32_t(f32x2_to_e4m3x2(q[2], q[3])) << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // One warp per (row, 512-column span of h).
 __global__ void __launch_bounds__(256)
@@ -389,7 +523,7 @@ __global__ void __launch_bounds__(256)
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
     }
     float s;
-    const uint4 q = quant16_group8(v, s);
+    const uint4 q = requant16_group8(v, s);
     if (!active) return;
     *reinterpret_cast<uint4*>(h + r * N + col) = q;
     if ((lane & 7) == 0) h_scale[r * G + g] = s;

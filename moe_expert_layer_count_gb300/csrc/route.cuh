@@ -16,10 +16,12 @@ int scatter_slots_per_cta(int64_t n);
 int launch_count(const int32_t* ids, int64_t n, const int32_t* expert_map, int E, int El, int32_t* counts,
                  int32_t* err_count, int num_sms, cudaStream_t stream);
 
+// counts_in NULL: the experts' slot counts are derived by the scatter's own histogram
+// pass and written to counts_out (bad ids then added to err_count, if not NULL).
 int launch_scatter(const uint16_t* x, int64_t M, int K, const int32_t* ids, const float* topk_weights, int topk,
-                   const int32_t* expert_map, int E, int El, const int32_t* counts, int apply_on_input, int quant,
-                   void* a_out, float* a_scale, int32_t* expert_offsets, int32_t* src2dst, int32_t* hist,
-                   cudaStream_t stream);
+                   const int32_t* expert_map, int E, int El, const int32_t* counts_in, int32_t* counts_out,
+                   int32_t* err_count, int apply_on_input, int quant, void* a_out, float* a_scale,
+                   int32_t* expert_offsets, int32_t* src2dst, int32_t* hist, cudaStream_t stream);
 
 int launch_gather(const uint16_t* y, const int32_t* src2dst, const float* topk_weights, int64_t M, int topk, int K,
                   int apply_on_input, uint16_t* out, cudaStream_t stream);

@@ -171,7 +171,7 @@ def test_silu_mul_quant(N, counts):
     Href, hsref = oracle.silu_mul_quant(c1, offs, counts)
     rows = np.concatenate([np.arange(offs[l], offs[l] + counts[l]) for l in range(len(counts))])
     gh, ghs = host(h)[rows], host(hs)[rows]
-    # fp32 SiLU on the GPU vs fp64 in the oracle: scales within a few ulp, codes within 1 step
-    np.testing.assert_allclose(ghs, hsref[rows], rtol=4e-7, atol=0)
+    # fast fp32 SiLU on the GPU vs fp64 in the oracle: scales within a few ulp, codes within 1 step
+    np.testing.assert_allclose(ghs, hsref[rows], rtol=2e-6, atol=0)
     d = e4m3_ulp_diff(gh, Href[rows])
     assert d.max() <= 1 and (d == 0).mean() >= 0.999
