@@ -66,6 +66,7 @@ def algorithmic(li, counts_per_chunk):
     n_slots = M * topk
     a = {}
     a["count_bytes"] = n_slots * 4 + (wl.E * 4 if wl.local_experts else 0)
+    # scatter: ids read (counting + ranking), x read once, FP8 rows + scales written, src2dst
     a["scatter_bytes"] = M * K * 2 + R * K + R * (K // 128) * 4 + n_slots * 4 * 2
     a["gather_bytes"] = R * K * 2 + M * K * 2 + n_slots * 8
     if N:
@@ -201,9 +202,8 @@ def run_ours(args, rank, world, local_rank):
                                      quant=moe.MOE_QUANT_NONE)
 
         def step():
-            moe.moe_count_expert_tokens(ids, E, El, emap, expert_num_tokens=cnt)
             moe.moe_scatter(x, ids, tw, E, El, cnt, emap, rp_cap=cap, a_out=A, a_scale=SA, expert_offsets=offs,
-                            src2dst=s2d, workspace=sws)
+                            src2dst=s2d, workspace=sws, count_here=True)
             moe.moe_gather_weight_reduce(Y, s2d, tw, out=out)
 
     # per-chunk counts (host side, for the algorithmic work only)
@@ -308,8 +308,8 @@ def kernel_breakdown(moe, torch, stream, li, x, ids, tw, emap, dev, args, permut
         HS = torch.empty(cap, N // 128, dtype=torch.float32, device=dev)
         fused = FUSED_SILU
         C1 = None if fused else torch.empty(cap, 2 * N, dtype=torch.float32, device=dev)
-    stages = ["count", "scatter"] + ([] if permute_only else (["gemm1"] + ([] if FUSED_SILU else ["silu"]) +
-                                                               ["gemm2"])) + ["gather"]
+    stages = ["scatter"] + ([] if permute_only else (["gemm1"] + ([] if FUSED_SILU else ["silu"]) +
+                                                      ["gemm2"])) + ["gather"]
     reps = max(3, min(args.steps, 20))
     times = {s: 0.0 for s in stages}
     launches = {s: 0 for s in stages}
@@ -328,14 +328,12 @@ def kernel_breakdown(moe, torch, stream, li, x, ids, tw, emap, dev, args, permut
             n0 = moe.moe_kernel_launch_count()
             marks = []
             e[0].record(stream)
-            moe.moe_count_expert_tokens(ii, E, El, emap, expert_num_tokens=cnt)
+            # the count step runs inside the scatter's histogram pass, as in the chunk loop
+            moe.moe_scatter(xi, ii, wi, E, El, cnt, emap, rp_cap=capc, a_out=A[:capc], a_scale=SA[:capc],
+                            expert_offsets=offs, src2dst=s2d[:Mc], workspace=sws, count_here=True)
             marks.append(moe.moe_kernel_launch_count())
             e[1].record(stream)
-            moe.moe_scatter(xi, ii, wi, E, El, cnt, emap, rp_cap=capc, a_out=A[:capc], a_scale=SA[:capc],
-                            expert_offsets=offs, src2dst=s2d[:Mc], workspace=sws)
-            marks.append(moe.moe_kernel_launch_count())
-            e[2].record(stream)
-            j = 2
+            j = 1
             if permute_only:
                 Yv = Y[:capc]
             else:
@@ -378,7 +376,7 @@ def kernel_breakdown(moe, torch, stream, li, x, ids, tw, emap, dev, args, permut
 
 def roofline(kern, work, pk, wl):
     t = kern["table"]
-    for s, key in (("count", "count_bytes"), ("scatter", "scatter_bytes"), ("gather", "gather_bytes")):
+    for s, key in (("scatter", "scatter_bytes"), ("gather", "gather_bytes")):
         if s in t and t[s]["us_per_step"] > 0:
             t[s]["GB/s"] = round(work[key] / (t[s]["us_per_step"] * 1e-6) / 1e9, 1)
             t[s]["hbm_frac"] = round(t[s]["GB/s"] / pk["hbm"], 4)

@@ -119,7 +119,12 @@ MOE_API int moe_count_expert_tokens(const int32_t* topk_ids, int64_t M, int topk
  *   topk_ids          int32 [M, topk];  topk_weights fp32 [M, topk] (read only when
  *                     apply_router_weight_on_input != 0: the copied row is then
  *                     bf16(x_t * w[t,k]), [P2] Changes)
- *   expert_num_tokens int32 [El], as written by moe_count_expert_tokens for the same ids
+ *   expert_num_tokens int32 [El]. count_here == 0: an input, as written by
+ *                     moe_count_expert_tokens for the same ids. count_here != 0: an
+ *                     output -- the scatter's own histogram pass counts the slots (the
+ *                     count step fused into the scatter, as the chunk loop does) and
+ *                     writes the same values moe_count_expert_tokens would; bad ids are
+ *                     then added to *err_count (when not NULL)
  *   quant             MOE_QUANT_FP8_1X128: a_out e4m3 [rp_cap, K] and a_scale fp32
  *                     [rp_cap, K/128] with scale = amax/448 per 1x128 group (fp32 IEEE
  *                     division), code = e4m3(x/scale) rounded to nearest-even and
@@ -132,9 +137,10 @@ MOE_API int moe_count_expert_tokens(const int32_t* topk_ids, int64_t M, int topk
  * The permutation is the unique stable order: deterministic, independent of timing. */
 MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32_t* topk_ids,
                         const float* topk_weights, int topk, const int32_t* expert_map, int E,
-                        int local_num_experts, const int32_t* expert_num_tokens, int apply_router_weight_on_input,
-                        int quant, void* a_out, float* a_scale, int32_t* expert_offsets, int32_t* src2dst,
-                        int64_t rp_cap, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+                        int local_num_experts, int32_t* expert_num_tokens, int count_here, int32_t* err_count,
+                        int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
+                        int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, void* workspace,
+                        size_t workspace_bytes, moe_stream_t stream);
 
 /* moe_scatter without a workspace argument, for callers that cannot allocate device
  * memory: for example an inference engine that plans every device buffer once at
@@ -142,7 +148,8 @@ MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32
  * device and may fail when memory is fragmented), or a host runtime that only passes
  * input and output buffers. The vLLM pages have no counterpart: this is an interface
  * convenience of this library, not a step of the method.
- * Arguments and results are those of moe_scatter (minus workspace/workspace_bytes).
+ * Arguments and results are those of moe_scatter with count_here = 0 (expert_num_tokens
+ * is an input), minus workspace/workspace_bytes.
  * The scratch it needs (per-block expert histograms) is a fixed array of 65536 int32
  * (256 KiB) in this library's own device memory, held by every GPU that loads the
  * library until the process exits. A problem needing more -- (number of scatter blocks)

@@ -58,8 +58,8 @@ SIGNATURES = {
     "moe_scatter_workspace_size": ([_i64, _int, _int], _sz),
     "moe_workspace_size": ([_i64, _int, _int, _int, _int], _sz),
     "moe_count_expert_tokens": ([_p, _i64, _int, _p, _int, _int, _p, _p, _p], _int),
-    "moe_scatter": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _int, _p, _p, _p, _p, _i64,
-                     _p, _sz, _p], _int),
+    "moe_scatter": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _p, _int, _int, _p, _p, _p, _p,
+                     _i64, _p, _sz, _p], _int),
     "moe_scatter_noalloc": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _int, _p, _p, _p, _p, _i64,
                              _p], _int),
     "moe_grouped_gemm_fp8": ([_p, _p, _p, _p, _p, _int, _i64, _int, _int, _int, _p, _p, _p], _int),
@@ -145,9 +145,10 @@ def moe_count_expert_tokens(topk_ids, E, local_num_experts, expert_map=None, exp
 def moe_scatter(hidden_states, topk_ids, topk_weights, E, local_num_experts, expert_num_tokens,
                 expert_map=None, apply_router_weight_on_input=False, quant=MOE_QUANT_FP8_1X128,
                 rp_cap=None, a_out=None, a_scale=None, expert_offsets=None, src2dst=None,
-                workspace=None, stream=None):
+                workspace=None, count_here=False, err_count=None, stream=None):
     """Permute rows into expert-contiguous, 128-aligned blocks (+ FP8 1x128 quant).
-    Returns (a_out, a_scale, expert_offsets, src2dst)."""
+    With count_here, expert_num_tokens is an output (the count step fused into the
+    scatter). Returns (a_out, a_scale, expert_offsets, src2dst)."""
     _dt(hidden_states, torch.bfloat16, "hidden_states")
     _dt(topk_ids, torch.int32, "topk_ids")
     _dt(topk_weights, torch.float32, "topk_weights")
@@ -168,8 +169,9 @@ def moe_scatter(hidden_states, topk_ids, topk_weights, E, local_num_experts, exp
         workspace = torch.empty(moe_scatter_workspace_size(M, topk, El), dtype=torch.uint8, device=dev)
     _check("moe_scatter", lib().moe_scatter(
         _ptr(hidden_states), M, K, _ptr(topk_ids), _ptr(topk_weights), topk, _ptr(expert_map), E, El,
-        _ptr(expert_num_tokens), int(bool(apply_router_weight_on_input)), quant, _ptr(a_out), _ptr(a_scale),
-        _ptr(expert_offsets), _ptr(src2dst), cap, _ptr(workspace), workspace.numel(), _stream(stream)))
+        _ptr(expert_num_tokens), int(bool(count_here)), _ptr(err_count), int(bool(apply_router_weight_on_input)),
+        quant, _ptr(a_out), _ptr(a_scale), _ptr(expert_offsets), _ptr(src2dst), cap, _ptr(workspace),
+        workspace.numel(), _stream(stream)))
     return a_out, a_scale, expert_offsets, src2dst
 
 

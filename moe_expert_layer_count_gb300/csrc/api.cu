@@ -130,8 +130,9 @@ MOE_API int moe_count_expert_tokens(const int32_t* topk_ids, int64_t M, int topk
 
 MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32_t* topk_ids,
                         const float* topk_weights, int topk, const int32_t* expert_map, int E, int local_num_experts,
-                        const int32_t* expert_num_tokens, int apply_router_weight_on_input, int quant, void* a_out,
-                        float* a_scale, int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, void* workspace,
+                        int32_t* expert_num_tokens, int count_here, int32_t* err_count,
+                        int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
+                        int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, void* workspace,
                         size_t workspace_bytes, moe_stream_t stream) {
     if (!routing_args_ok(M, topk, E, local_num_experts) || K <= 0 || K % kGroup || !expert_num_tokens ||
         !expert_offsets || (quant != MOE_QUANT_NONE && quant != MOE_QUANT_FP8_1X128))
@@ -148,9 +149,10 @@ MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32
     if (multi && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if (int st = check_device(nullptr)) return st;
     return launch_scatter(static_cast<const uint16_t*>(hidden_states), M, K, topk_ids, topk_weights, topk, expert_map, E,
-                          local_num_experts, expert_num_tokens, nullptr, nullptr, apply_router_weight_on_input ? 1 : 0,
-                          quant, a_out, a_scale, expert_offsets, src2dst, static_cast<int32_t*>(workspace),
-                          (cudaStream_t)stream);
+                          local_num_experts, count_here ? nullptr : expert_num_tokens,
+                          count_here ? expert_num_tokens : nullptr, count_here ? err_count : nullptr,
+                          apply_router_weight_on_input ? 1 : 0, quant, a_out, a_scale, expert_offsets, src2dst,
+                          static_cast<int32_t*>(workspace), (cudaStream_t)stream);
 }
 
 MOE_API int moe_grouped_gemm_fp8(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,

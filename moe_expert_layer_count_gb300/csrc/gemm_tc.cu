@@ -66,10 +66,38 @@ struct __align__(8) Tail {
     int abort;
 };
 
+constexpr int kStageRowBytes = 64;                       // per-warp output staging: 32 rows x 64 bytes
+constexpr int kStageWarpBytes = 32 * kStageRowBytes;
+
 template <int BN>
 constexpr size_t smem_bytes(int El) {
     return 1024 + (size_t)Cfg<BN>::kStages * Cfg<BN>::kStageBytes + sizeof(Tail) + 2 * 2 * 128 * sizeof(float) +
-           (size_t)(El + 1) * sizeof(int32_t);
+           (size_t)(El + 1) * sizeof(int32_t) + 128 + (size_t)kEpiWarps * kStageWarpBytes;
+}
+
+// Byte offset of 16-byte chunk c (0..3) of row r (0..31) in a warp's 32 x 64-byte
+// staging buffer. The XOR spreads the 8 rows of every 512-byte group over all 32 banks,
+// so both the row-per-lane writes and the 8-rows-per-instruction reads are conflict-free.
+__device__ __forceinline__ uint32_t stage_off(int r, int c) {
+    return (uint32_t)(r * kStageRowBytes + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+// Writes 64 bytes per lane (lane = row of the warp's 32-row slab) to global memory as
+// rows of 64 contiguous bytes: lane l's 4 chunks go through the staging buffer, then
+// each store instruction covers 8 rows x 64 bytes. `dst_row0` points at the slab's
+// first row (64 bytes wide here), rows `pitch` bytes apart.
+__device__ __forceinline__ void store_rows64(uint8_t* stage, int lane, const uint4 (&v)[4], uint8_t* dst_row0,
+                                             int64_t pitch) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(stage + stage_off(lane, c)) = v[c];
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = i * 8 + (lane >> 2), c = lane & 3;
+        const uint4 q = *reinterpret_cast<const uint4*>(stage + stage_off(r, c));
+        *reinterpret_cast<uint4*>(dst_row0 + r * pitch + c * 16) = q;
+    }
+    __syncwarp();
 }
 
 // Bounded wait on an mbarrier phase. With check_abort, returns false as soon as another
@@ -113,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Tail* st = reinterpret_cast<Tail*>(smem + C::kStages * C::kStageBytes);
     float* s_amax = reinterpret_cast<float*>(st + 1);  // [2 parities][2 warpgroups][128 rows]
     int32_t* s_off = reinterpret_cast<int32_t*>(s_amax + 2 * 2 * 128);
+    uint8_t* s_stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_off + El + 1) + 127) & ~uintptr_t(127));
     volatile int* abort = &st->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -312,25 +341,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                         d[j] = s == 0.f ? 0.f : (fast ? div_rn_by(acc[4 * q + j], s, rs) : __fdiv_rn(acc[4 * q + j], s));
                     w[q] = uint32_t(f32x2_to_e4m3x2(d[0], d[1])) | (uint32_t(f32x2_to_e4m3x2(d[2], d[3])) << 16);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + r * N + nt * 128 + wg * 64);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                const uint4 v4[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
+                                     make_uint4(w[8], w[9], w[10], w[11]), make_uint4(w[12], w[13], w[14], w[15])};
+                store_rows64(s_stage + warp * kStageWarpBytes, lane, v4,
+                             static_cast<uint8_t*>(out) + (r - lane) * N + nt * 128 + wg * 64, N);
                 if (wg == 0) out_scale[r * (N / 128) + nt] = s;
             } else if (EPI == MOE_EPI_F32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + r * n_out + nt * BN + wg * C::kCols);
+                // 16 fp32 columns (64 bytes) per round
+                uint8_t* base = reinterpret_cast<uint8_t*>(static_cast<float*>(out) + (r - lane) * n_out + nt * BN +
+                                                           wg * C::kCols);
 #pragma unroll
-                for (int q = 0; q < C::kCols / 4; ++q)
-                    dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                for (int q = 0; q < C::kCols / 16; ++q) {
+                    uint4 v4[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v4[c] = make_uint4(__float_as_uint(acc[16 * q + 4 * c]), __float_as_uint(acc[16 * q + 4 * c + 1]),
+                                           __float_as_uint(acc[16 * q + 4 * c + 2]),
+                                           __float_as_uint(acc[16 * q + 4 * c + 3]));
+                    store_rows64(s_stage + warp * kStageWarpBytes, lane, v4, base + q * 64, (int64_t)n_out * 4);
+                }
             } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + r * n_out + nt * BN + wg * C::kCols);
+                // 32 bf16 columns (64 bytes) per round
+                uint8_t* base = reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(out) + (r - lane) * n_out +
+                                                           nt * BN + wg * C::kCols);
 #pragma unroll
-                for (int q = 0; q < C::kCols / 8; ++q) {
-                    uint32_t w[4];
+                for (int q = 0; q < C::kCols / 32; ++q) {
+                    uint4 v4[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = uint32_t(f32_to_bf16_bits(acc[8 * q + 2 * e])) |
-                               (uint32_t(f32_to_bf16_bits(acc[8 * q + 2 * e + 1])) << 16);
-                    dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = uint32_t(f32_to_bf16_bits(acc[32 * q + 8 * c + 2 * e])) |
+                                   (uint32_t(f32_to_bf16_bits(acc[32 * q + 8 * c + 2 * e + 1])) << 16);
+                        v4[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    store_rows64(s_stage + warp * kStageWarpBytes, lane, v4, base + q * 64, (int64_t)n_out * 2);
                 }
             }
         }

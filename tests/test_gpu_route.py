@@ -95,6 +95,31 @@ def test_scatter_bit_exact(M, topk, E, local):
     compare_scatter(x, ids, w, E, El, m)
 
 
+@pytest.mark.parametrize("M,topk,E,local", [(1, 8, 128, None), (200, 8, 128, "random"), (5000, 8, 128, "half"),
+                                            (70000, 8, 128, None), (300, 8, 128, "none_local")])
+def test_scatter_counting_fused(M, topk, E, local):
+    """count_here: the scatter's histogram pass yields the counts (and bad-id total) of
+    moe_count_expert_tokens, and the same offsets, src2dst and FP8 rows."""
+    K = 256
+    ids, w, m, El = routing(M, topk, E, _local(E, local), seed=M + 7, zipf=1.2)
+    ids[0, 0] = E + 5  # one bad id
+    x = mi.hidden_states(M, K, seed=M)
+    md = None if m is None else dev(m)
+    cnt = torch.full((El,), -3, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a, sa, offs, s2d = moe.moe_scatter(dev(x), dev(ids), dev(w), E, El, cnt, md, count_here=True, err_count=err)
+    torch.cuda.synchronize()
+    r = oracle.scatter(x, ids, w, E, El, m)
+    assert (host(cnt) == r["counts"]).all()
+    assert int(err.item()) == r["bad"] == 1
+    assert (host(offs) == r["offsets"]).all()
+    assert (host(s2d) == r["src2dst"]).all()
+    rows = r["src2dst"].reshape(-1)
+    rows = rows[rows >= 0]
+    assert (host(a)[rows] == r["a"][rows]).all()
+    assert (host(sa)[rows].view(np.uint32) == r["a_scale"][rows].view(np.uint32)).all()
+
+
 @pytest.mark.parametrize("quant", [True, False])
 @pytest.mark.parametrize("apply_on_input", [False, True])
 def test_scatter_variants(quant, apply_on_input):
