@@ -47,6 +47,23 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(ms, world, device):
+    """The step time of the job: the slowest rank's (all ranks get it)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, ms_per_step):
+    """Whole-job tokens/s: every rank processes its own batch of tokens_per_rank
+    (weak scaling), in the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -236,9 +253,7 @@ def run_ours(args, rank, world, local_rank):
     ms = e0.elapsed_time(e1) / args.steps
     if world > 1:
         dist.barrier()
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     clk.stop()
 
     # ---- per-kernel breakdown on the same stream (separate loop, same calls) ----
@@ -250,8 +265,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e = end_to_end(moe, torch, stream, li, dev, args, step, x, ids, tw, out)
 
-    tokens = M * world
-    value = tokens / (ms / 1e3)
+    value = job_throughput(M, world, ms)
     pk = peaks()
     roof = roofline(kern, work, pk, wl)
     line = {

@@ -72,7 +72,7 @@ constexpr int kStageWarpBytes = 32 * kStageRowBytes;
 template <int BN>
 constexpr size_t smem_bytes(int El) {
     return 1024 + (size_t)Cfg<BN>::kStages * Cfg<BN>::kStageBytes + sizeof(Tail) + 2 * 2 * 128 * sizeof(float) +
-           (size_t)(El + 1) * sizeof(int32_t) + 128 + (size_t)kEpiWarps * kStageWarpBytes;
+           (size_t)(El + 1) * sizeof(int32_t) + 1024 + (size_t)kEpiWarps * kStageWarpBytes;
 }
 
 // Byte offset of 16-byte chunk c (0..3) of row r (0..31) in a warp's 32 x 64-byte
@@ -82,22 +82,23 @@ __device__ __forceinline__ uint32_t stage_off(int r, int c) {
     return (uint32_t)(r * kStageRowBytes + ((c ^ ((r >> 1) & 3)) << 4));
 }
 
-// Writes 64 bytes per lane (lane = row of the warp's 32-row slab) to global memory as
-// rows of 64 contiguous bytes: lane l's 4 chunks go through the staging buffer, then
-// each store instruction covers 8 rows x 64 bytes. `dst_row0` points at the slab's
-// first row (64 bytes wide here), rows `pitch` bytes apart.
-__device__ __forceinline__ void store_rows64(uint8_t* stage, int lane, const uint4 (&v)[4], uint8_t* dst_row0,
-                                             int64_t pitch) {
+// Stores a 32-row x 64-byte box of the output (lane = row of the warp's 32-row slab,
+// 64 bytes per lane) with one TMA store: the lanes write the swizzled staging buffer
+// (the layout above is exactly TMA's 64-byte swizzle), then lane 0 issues the bulk
+// store at tensor coordinates (x, y). The buffer is reused only after the previous
+// store has read it.
+__device__ __forceinline__ void store_box64(uint8_t* stage, int lane, const uint4 (&v)[4], const CUtensorMap* tm,
+                                            int32_t x, int32_t y) {
+    if (lane == 0) ptx::bulk_wait_read0();
+    __syncwarp();
 #pragma unroll
     for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(stage + stage_off(lane, c)) = v[c];
+    ptx::fence_proxy_async_smem();
     __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = i * 8 + (lane >> 2), c = lane & 3;
-        const uint4 q = *reinterpret_cast<const uint4*>(stage + stage_off(r, c));
-        *reinterpret_cast<uint4*>(dst_row0 + r * pitch + c * 16) = q;
+    if (lane == 0) {
+        ptx::tma_store_2d(tm, ptx::smem_addr(stage), x, y);
+        ptx::bulk_commit();
     }
-    __syncwarp();
 }
 
 // Bounded wait on an mbarrier phase. With check_abort, returns false as soon as another
@@ -131,7 +132,7 @@ __device__ __forceinline__ int expert_of(const int32_t* s_off, int El, int row0)
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const float* __restrict__ sa, const float* __restrict__ sw, const int32_t* __restrict__ offsets,
+                   const __grid_constant__ CUtensorMap tmO, const float* __restrict__ sa, const float* __restrict__ sw, const int32_t* __restrict__ offsets,
                    int El, int n_out, int k_in, void* __restrict__ out, float* __restrict__ out_scale) {
     using C = Cfg<BN>;
     constexpr bool kSilu = EPI == MOE_EPI_SILU_MUL_QUANT;
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Tail* st = reinterpret_cast<Tail*>(smem + C::kStages * C::kStageBytes);
     float* s_amax = reinterpret_cast<float*>(st + 1);  // [2 parities][2 warpgroups][128 rows]
     int32_t* s_off = reinterpret_cast<int32_t*>(s_amax + 2 * 2 * 128);
-    uint8_t* s_stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_off + El + 1) + 127) & ~uintptr_t(127));
+    uint8_t* s_stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_off + El + 1) + 1023) & ~uintptr_t(1023));
     volatile int* abort = &st->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
+        ptx::prefetch_tmap(&tmO);
     }
     __syncthreads();
     ptx::tc_fence_after();
@@ -343,13 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint4 v4[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
                                      make_uint4(w[8], w[9], w[10], w[11]), make_uint4(w[12], w[13], w[14], w[15])};
-                store_rows64(s_stage + warp * kStageWarpBytes, lane, v4,
-                             static_cast<uint8_t*>(out) + (r - lane) * N + nt * 128 + wg * 64, N);
+                store_box64(s_stage + warp * kStageWarpBytes, lane, v4, &tmO, nt * 128 + wg * 64, (int)(r - lane));
                 if (wg == 0) out_scale[r * (N / 128) + nt] = s;
             } else if (EPI == MOE_EPI_F32) {
                 // 16 fp32 columns (64 bytes) per round
-                uint8_t* base = reinterpret_cast<uint8_t*>(static_cast<float*>(out) + (r - lane) * n_out + nt * BN +
-                                                           wg * C::kCols);
 #pragma unroll
                 for (int q = 0; q < C::kCols / 16; ++q) {
                     uint4 v4[4];
@@ -358,12 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         v4[c] = make_uint4(__float_as_uint(acc[16 * q + 4 * c]), __float_as_uint(acc[16 * q + 4 * c + 1]),
                                            __float_as_uint(acc[16 * q + 4 * c + 2]),
                                            __float_as_uint(acc[16 * q + 4 * c + 3]));
-                    store_rows64(s_stage + warp * kStageWarpBytes, lane, v4, base + q * 64, (int64_t)n_out * 4);
+                    store_box64(s_stage + warp * kStageWarpBytes, lane, v4, &tmO, nt * BN + wg * C::kCols + q * 16,
+                                (int)(r - lane));
                 }
             } else {
                 // 32 bf16 columns (64 bytes) per round
-                uint8_t* base = reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(out) + (r - lane) * n_out +
-                                                           nt * BN + wg * C::kCols);
 #pragma unroll
                 for (int q = 0; q < C::kCols / 32; ++q) {
                     uint4 v4[4];
@@ -376,11 +374,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    (uint32_t(f32_to_bf16_bits(acc[32 * q + 8 * c + 2 * e + 1])) << 16);
                         v4[c] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    store_rows64(s_stage + warp * kStageWarpBytes, lane, v4, base + q * 64, (int64_t)n_out * 2);
+                    store_box64(s_stage + warp * kStageWarpBytes, lane, v4, &tmO, nt * BN + wg * C::kCols + q * 32,
+                                (int)(r - lane));
                 }
             }
         }
     }
+    if (warp < kEpiWarps && lane == 0) ptx::bulk_wait0();  // this warp's output stores have completed
     __syncthreads();
     if (warp == kMmaWarp) {
         __syncwarp();
@@ -417,8 +417,25 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output tensor [rows, cols] of `esize`-byte elements, stored in boxes of 32 rows x 64
+// bytes with 64-byte swizzling (the epilogue's staging layout).
+bool make_out_tmap(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, int esize) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const CUtensorMapDataType dt = esize == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * (uint64_t)esize};
+    const cuuint32_t box[2] = {(cuuint32_t)(kStageRowBytes / esize), 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, int EPI>
-int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* w_scale,
+int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const float* a_scale,
+              const float* w_scale,
               const int32_t* offsets, int El, int64_t rp_cap, int n_out, int k_in, void* out, float* out_scale,
               int num_sms, cudaStream_t stream) {
     const size_t smem = smem_bytes<BN>(El);
@@ -433,8 +450,8 @@ int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale
     const int64_t max_tiles = rp_cap / kBM * n_tiles;
     const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid < 1) return MOE_OK;
-    gemm_tc_kernel<BN, EPI><<<grid, kThreads, smem, stream>>>(ta, tb, a_scale, w_scale, offsets, El, n_out, k_in, out,
-                                                             out_scale);
+    gemm_tc_kernel<BN, EPI><<<grid, kThreads, smem, stream>>>(ta, tb, to, a_scale, w_scale, offsets, El, n_out, k_in,
+                                                             out, out_scale);
     note_launches(1);
     return launch_status();
 }
@@ -446,23 +463,26 @@ int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w
                         void* out, float* out_scale, int num_sms, cudaStream_t stream) {
     if (rp_cap == 0) return MOE_OK;
     const bool bn256 = n_out % 256 == 0;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, to;
+    const int o_cols = epilogue == MOE_EPI_SILU_MUL_QUANT ? n_out / 2 : n_out;
+    const int o_esize = epilogue == MOE_EPI_SILU_MUL_QUANT ? 1 : epilogue == MOE_EPI_F32 ? 4 : 2;
     if (!make_tmap(&ta, a, (uint64_t)k_in, (uint64_t)rp_cap, kBM) ||
-        !make_tmap(&tb, w, (uint64_t)k_in, (uint64_t)El * n_out, kBoxRows))
+        !make_tmap(&tb, w, (uint64_t)k_in, (uint64_t)El * n_out, kBoxRows) ||
+        !make_out_tmap(&to, out, (uint64_t)o_cols, (uint64_t)rp_cap, o_esize))
         return MOE_ERR_CUDA;
     switch (epilogue) {
         case MOE_EPI_SILU_MUL_QUANT:
-            return launch_tc<256, MOE_EPI_SILU_MUL_QUANT>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+            return launch_tc<256, MOE_EPI_SILU_MUL_QUANT>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
                                                           k_in, out, out_scale, num_sms, stream);
         case MOE_EPI_F32:
-            return bn256 ? launch_tc<256, MOE_EPI_F32>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+            return bn256 ? launch_tc<256, MOE_EPI_F32>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
                                                        k_in, out, out_scale, num_sms, stream)
-                         : launch_tc<128, MOE_EPI_F32>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+                         : launch_tc<128, MOE_EPI_F32>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
                                                        k_in, out, out_scale, num_sms, stream);
         default:
-            return bn256 ? launch_tc<256, MOE_EPI_BF16>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+            return bn256 ? launch_tc<256, MOE_EPI_BF16>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
                                                         k_in, out, out_scale, num_sms, stream)
-                         : launch_tc<128, MOE_EPI_BF16>(ta, tb, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+                         : launch_tc<128, MOE_EPI_BF16>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
                                                         k_in, out, out_scale, num_sms, stream);
     }
 }
