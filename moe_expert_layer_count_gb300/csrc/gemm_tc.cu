@@ -331,18 +331,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!got) { ok = false; break; }
                 amax = fmaxf(xa[row_in_tile], xa[128 + row_in_tile]);
                 const float s = __fdiv_rn(amax, 448.0f);
-                // code = e4m3(h / s) with the correctly rounded quotient
-                const bool fast = s >= 1e-30f;
-                const float rs = fast ? __frcp_rn(s) : 0.f;
+                // code = e4m3(h / s) with the correctly rounded quotient; the branch is per
+                // row (uniform over the loop), so only one division path is executed
+                if (s == 0.f) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+                } else if (s >= 1e-30f) {
+                    const float rs = __frcp_rn(s);
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) acc[j] = div_rn_by(acc[j], s, rs);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) acc[j] = __fdiv_rn(acc[j], s);
+                }
                 uint32_t w[16];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    float d[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        d[j] = s == 0.f ? 0.f : (fast ? div_rn_by(acc[4 * q + j], s, rs) : __fdiv_rn(acc[4 * q + j], s));
-                    w[q] = uint32_t(f32x2_to_e4m3x2(d[0], d[1])) | (uint32_t(f32x2_to_e4m3x2(d[2], d[3])) << 16);
-                }
+                for (int q = 0; q < 16; ++q)
+                    w[q] = uint32_t(f32x2_to_e4m3x2(acc[4 * q], acc[4 * q + 1])) |
+                           (uint32_t(f32x2_to_e4m3x2(acc[4 * q + 2], acc[4 * q + 3])) << 16);
                 const uint4 v4[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
                                      make_uint4(w[8], w[9], w[10], w[11]), make_uint4(w[12], w[13], w[14], w[15])};
                 store_box64(s_stage + warp * kStageWarpBytes, lane, v4, &tmO, nt * 128 + wg * 64, (int)(r - lane));

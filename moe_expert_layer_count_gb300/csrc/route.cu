@@ -478,17 +478,22 @@ __device__ __forceinline__ uint4 requant16_group8(const float (&v)[16], float& s
     for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = __fdiv_rn(amax, 448.0f);
     scale_out = s;
-    const bool fast = s >= 1e-30f;  // 1/s finite and normal
-    const float r = fast ? __frcp_rn(s) : 0.f;
+    float q[16];
+    if (s == 0.f) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) q[j] = 0.f;
+    } else if (s >= 1e-30f) {  // 1/s finite and normal
+        const float r = __frcp_rn(s);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) q[j] = div_rn_by(v[j], s, r);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(v[j], s);
+    }
     uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float q[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            q[j] = s == 0.f ? 0.f : (fast ? div_rn_by(v[4 * i + j], s, r) : __fdiv_rn(v[4 * i + j], s));
-        w[i] = uint32_t(f32x2_to_e4m3x2(q[0], q[1])) | (uint32_t(f32x2_to_e4m3x2(q[2], q[3])) << 16);
-    }
+    for (int i = 0; i < 4; ++i)
+        w[i] = uint32_t(f32x2_to_e4m3x2(q[4 * i], q[4 * i + 1])) | (uint32_t(f32x2_to_e4m3x2(q[4 * i + 2], q[4 * i + 3])) << 16);
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
