@@ -146,7 +146,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &st->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i <= El; i += kThreads) s_off[i] = __ldg(offsets + i);
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(ptx::smem_addr(&st->full[s]), 1);
@@ -171,6 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&tmB);
         ptx::prefetch_tmap(&tmO);
     }
+    // the prologue above overlaps the previous kernel's end; global memory only after this
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i <= El; i += kThreads) s_off[i] = __ldg(offsets + i);
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = st->tmem_base;
@@ -456,8 +459,7 @@ int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& t
     const int64_t max_tiles = rp_cap / kBM * n_tiles;
     const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid < 1) return MOE_OK;
-    gemm_tc_kernel<BN, EPI><<<grid, kThreads, smem, stream>>>(ta, tb, to, a_scale, w_scale, offsets, El, n_out, k_in,
-                                                             out, out_scale);
+    launch_k(gemm_tc_kernel<BN, EPI>, grid, kThreads, smem, stream, ta, tb, to, a_scale, w_scale, offsets, El, n_out, k_in, out, out_scale);
     note_launches(1);
     return launch_status();
 }

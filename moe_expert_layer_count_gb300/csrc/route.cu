@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kThreads)
     constexpr int kVec = 4;  // int4 loads in flight per thread
     extern __shared__ int32_t hist[];
     for (int l = threadIdx.x; l < El; l += kThreads) hist[l] = 0;
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
     const int lane = threadIdx.x & 31;
     int bad = 0;
@@ -74,7 +76,7 @@ int launch_count(const int32_t* ids, int64_t n, const int32_t* expert_map, int E
                  int32_t* err_count, int num_sms, cudaStream_t stream) {
     const size_t smem = (size_t)El * sizeof(int32_t);
     if (n <= 16384) {  // one CTA, one batch of loads per thread: no memset needed
-        count_kernel<1024><<<1, 1024, smem, stream>>>(ids, n, expert_map, E, El, counts, err_count, 1);
+        launch_k(count_kernel<1024>, 1, 1024, smem, stream, ids, n, expert_map, E, El, counts, err_count, 1);
         note_launches(1);
         return launch_status();
     }
@@ -82,7 +84,7 @@ int launch_count(const int32_t* ids, int64_t n, const int32_t* expert_map, int E
     if (cudaMemsetAsync(counts, 0, (size_t)El * sizeof(int32_t), stream) != cudaSuccess) return MOE_ERR_CUDA;
     const int64_t want = (n + 4095) / 4096;
     const int grid = (int)(want < 4 * num_sms ? want : 4 * num_sms);
-    count_kernel<256><<<grid, 256, smem, stream>>>(ids, n, expert_map, E, El, counts, err_count, 0);
+    launch_k(count_kernel<256>, grid, 256, smem, stream, ids, n, expert_map, E, El, counts, err_count, 0);
     note_launches(1);
     return launch_status();
 }
@@ -126,6 +128,8 @@ __global__ void __launch_bounds__(kScatterThreads)
                         int El, int per_cta, int32_t* __restrict__ hist, int32_t* __restrict__ err_count) {
     extern __shared__ int32_t sh[];
     for (int l = threadIdx.x; l < El; l += kScatterThreads) sh[l] = 0;
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per_warp = per_cta / (kScatterThreads / 32);
@@ -170,6 +174,8 @@ __global__ void __launch_bounds__(kScatterThreads)
     const int64_t wbeg = (int64_t)blockIdx.x * per_cta + (int64_t)warp * per_warp;
     const int64_t wend = min(n, wbeg + per_warp);
     int bad = 0;
+    pdl_wait();
+    pdl_trigger();
     // the first round of this warp's slots, in flight while the histograms are summed
     int l0[kRound];
     load_round(ids, wbeg, wend, expert_map, E, El, lane, l0, bad);
@@ -305,6 +311,8 @@ __global__ void __launch_bounds__(256)
                         const float* __restrict__ topk_weights, int topk, int apply_on_input,
                         void* __restrict__ a_out, float* __restrict__ a_scale) {
     const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     const int spans = (K + 511) / 512;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (gw >= M * spans) return;
@@ -384,23 +392,18 @@ int launch_scatter(const uint16_t* x, int64_t M, int K, const int32_t* ids, cons
     const size_t smem_rank = (size_t)(3 * El + 1 + (kScatterThreads / 32) * El) * sizeof(int32_t);
     int launches = 0;
     if (grid > 1) {
-        scatter_hist_kernel<<<grid, kScatterThreads, (size_t)El * sizeof(int32_t), stream>>>(
-            ids, n, expert_map, E, El, per_cta, hist, counts_in ? nullptr : err_count);
+        launch_k(scatter_hist_kernel, grid, kScatterThreads, (size_t)El * sizeof(int32_t), stream, ids, n, expert_map, E, El, per_cta, hist, counts_in ? nullptr : err_count);
         ++launches;
     }
-    scatter_rank_kernel<<<grid < 1 ? 1 : grid, kScatterThreads, smem_rank, stream>>>(
-        ids, n, expert_map, E, El, per_cta, counts_in, hist, expert_offsets, src2dst, counts_out,
-        counts_in ? nullptr : err_count);
+    launch_k(scatter_rank_kernel, grid < 1 ? 1 : grid, kScatterThreads, smem_rank, stream, ids, n, expert_map, E, El, per_cta, counts_in, hist, expert_offsets, src2dst, counts_out, counts_in ? nullptr : err_count);
     ++launches;
     if (M > 0) {
         const int64_t warps = M * ((K + 511) / 512);
         const unsigned cgrid = (unsigned)((warps + 7) / 8);
         if (quant == MOE_QUANT_FP8_1X128)
-            scatter_copy_kernel<true><<<cgrid, 256, 0, stream>>>(x, M, K, src2dst, topk_weights, topk, apply_on_input,
-                                                                  a_out, a_scale);
+            launch_k(scatter_copy_kernel<true>, cgrid, 256, 0, stream, x, M, K, src2dst, topk_weights, topk, apply_on_input, a_out, a_scale);
         else
-            scatter_copy_kernel<false><<<cgrid, 256, 0, stream>>>(x, M, K, src2dst, topk_weights, topk,
-                                                                   apply_on_input, a_out, a_scale);
+            launch_k(scatter_copy_kernel<false>, cgrid, 256, 0, stream, x, M, K, src2dst, topk_weights, topk, apply_on_input, a_out, a_scale);
         ++launches;
     }
     note_launches(launches);
@@ -416,6 +419,8 @@ __global__ void __launch_bounds__(256)
                   const float* __restrict__ topk_weights, int64_t M, int topk, int K, int apply_on_input,
                   uint16_t* __restrict__ out) {
     const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     const int spans = (K + 255) / 256;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (gw >= M * spans) return;
@@ -461,8 +466,7 @@ int launch_gather(const uint16_t* y, const int32_t* src2dst, const float* topk_w
                   int apply_on_input, uint16_t* out, cudaStream_t stream) {
     if (M == 0) return MOE_OK;
     const int64_t warps = M * ((K + 255) / 256);
-    gather_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(y, src2dst, topk_weights, M, topk, K,
-                                                                     apply_on_input, out);
+    launch_k(gather_kernel, (unsigned)((warps + 7) / 8), 256, 0, stream, y, src2dst, topk_weights, M, topk, K, apply_on_input, out);
     note_launches(1);
     return launch_status();
 }
@@ -502,6 +506,8 @@ __global__ void __launch_bounds__(256)
     silu_mul_quant_kernel(const float* __restrict__ c1, const int32_t* __restrict__ expert_offsets, int El,
                           int64_t rp_cap, int N, uint8_t* __restrict__ h, float* __restrict__ h_scale) {
     const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     const int spans = (N + 511) / 512;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (gw >= rp_cap * spans) return;
@@ -538,8 +544,7 @@ int launch_silu_mul_quant(const float* c1, const int32_t* expert_offsets, int El
                           float* h_scale, cudaStream_t stream) {
     if (rp_cap == 0) return MOE_OK;
     const int64_t warps = rp_cap * ((N + 511) / 512);
-    silu_mul_quant_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(c1, expert_offsets, El, rp_cap, N, h,
-                                                                             h_scale);
+    launch_k(silu_mul_quant_kernel, (unsigned)((warps + 7) / 8), 256, 0, stream, c1, expert_offsets, El, rp_cap, N, h, h_scale);
     note_launches(1);
     return launch_status();
 }
