@@ -7,6 +7,11 @@
 // Design (one persistent CTA per SM, warp-specialised):
 //  * warp 8 (one thread) streams 128x128 A tiles and BNx128 W tiles into a ring of
 //    shared-memory stages with TMA (128-byte swizzle), one stage per 128-wide K block;
+//  * bf16/fp32 epilogues: warp 10 copies each K block's block scales (the 128 row
+//    scales of A, two W scales) into a ring of shared-memory slots with cp.async,
+//    running up to 8 K blocks ahead of the epilogue. The SiLU epilogue has no warp 10:
+//    each epilogue thread loads its row's scales itself, one K block ahead (measured
+//    faster for that GEMM, whose 16 K blocks per tile leave the loads time to land);
 //  * warp 9 (one thread) issues tcgen05.mma kind::f8f6f4 (M=128, N=BN, K=32, four per
 //    K block) into one of two TMEM accumulators, starting each K block from zero;
 //  * warps 0-7 (two warpgroups, each one TMEM lane = one row per thread, half of the
@@ -41,19 +46,42 @@ constexpr int kBK = 128;  // one K block: 128 fp8 = one 128-byte swizzled row
 constexpr int kEpiWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = (kEpiWarps + 2) * 32;
+constexpr int kScaleWarp = 10;
+
+// Whether an epilogue gets its block scales from the scale warp's ring, and the block
+// size that follows (at most 3 warps per SM sub-partition either way).
+template <int EPI>
+__host__ __device__ constexpr bool staged_scales() { return EPI != MOE_EPI_SILU_MUL_QUANT; }
+template <int EPI>
+__host__ __device__ constexpr int threads_of() { return (kEpiWarps + (staged_scales<EPI>() ? 3 : 2)) * 32; }
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kBoxRows = 64;  // W is loaded in 64-row TMA boxes
 
-template <int BN>
+template <int BN, int EPI>
 struct Cfg {
-    static constexpr int kStages = BN == 256 ? 4 : 6;
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = BN * kBK;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;
     static constexpr int kCols = BN / 2;  // accumulator columns per epilogue thread
+    // bf16 output leaves in 128-byte-wide boxes from a staging buffer that holds the
+    // warp's whole 32-row slab (all its stores of a tile go out without waiting); the
+    // other epilogues stage one 32 x 64-byte box per warp. The pipeline gets what
+    // shared memory is left.
+    static constexpr bool kWide = EPI == MOE_EPI_BF16;
+    static constexpr int kStageWarpBytes = kWide ? 32 * kCols * 2 : 32 * 64;
+    static constexpr int kStages = BN == 256 ? (kWide ? 3 : 4) : (kWide ? 5 : 6);
 };
+
+// Block scales of one K block of one tile: a_scale of the tile's 128 rows and the two
+// W scales its columns need (the two 128-column halves for BN = 256, the same value
+// twice for BN = 128).
+struct __align__(16) ScaleSlot {
+    float sa[kBM];
+    float sw[4];
+};
+// The scale warp fills it up to kScaleRing K blocks ahead of the epilogue.
+constexpr int kScaleRing = 8;
 
 struct __align__(8) Tail {
     uint64_t full[8];
@@ -61,18 +89,21 @@ struct __align__(8) Tail {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t amax_bar[2];
+    uint64_t sfull[kScaleRing];
+    uint64_t sempty[kScaleRing];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr int kStageRowBytes = 64;                       // per-warp output staging: 32 rows x 64 bytes
-constexpr int kStageWarpBytes = 32 * kStageRowBytes;
+constexpr int kStageRowBytes = 64;  // rows of the 64-byte-wide output boxes
 
-template <int BN>
+template <int BN, int EPI>
 constexpr size_t smem_bytes(int El) {
-    return 1024 + (size_t)Cfg<BN>::kStages * Cfg<BN>::kStageBytes + sizeof(Tail) + 2 * 2 * 128 * sizeof(float) +
-           (size_t)(El + 1) * sizeof(int32_t) + 1024 + (size_t)kEpiWarps * kStageWarpBytes;
+    using C = Cfg<BN, EPI>;
+    return 1024 + (size_t)C::kStages * C::kStageBytes + sizeof(Tail) + 16 + kScaleRing * sizeof(ScaleSlot) +
+           2 * 2 * 128 * sizeof(float) + (size_t)(El + 1) * sizeof(int32_t) + 1024 +
+           (size_t)kEpiWarps * C::kStageWarpBytes;
 }
 
 // Byte offset of 16-byte chunk c (0..3) of row r (0..31) in a warp's 32 x 64-byte
@@ -130,17 +161,19 @@ __device__ __forceinline__ int expert_of(const int32_t* s_off, int El, int row0)
 
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<EPI>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, const float* __restrict__ sa, const float* __restrict__ sw, const int32_t* __restrict__ offsets,
                    int El, int n_out, int k_in, void* __restrict__ out, float* __restrict__ out_scale) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, EPI>;
     constexpr bool kSilu = EPI == MOE_EPI_SILU_MUL_QUANT;
+    constexpr bool kStaged = staged_scales<EPI>();
     static_assert(!kSilu || BN == 256, "the SiLU epilogue pairs 128 gate with 128 up columns");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Tail* st = reinterpret_cast<Tail*>(smem + C::kStages * C::kStageBytes);
-    float* s_amax = reinterpret_cast<float*>(st + 1);  // [2 parities][2 warpgroups][128 rows]
+    ScaleSlot* s_scale = reinterpret_cast<ScaleSlot*>((reinterpret_cast<uintptr_t>(st + 1) + 15) & ~uintptr_t(15));
+    float* s_amax = reinterpret_cast<float*>(s_scale + kScaleRing);  // [2 parities][2 warpgroups][128 rows]
     int32_t* s_off = reinterpret_cast<int32_t*>(s_amax + 2 * 2 * 128);
     uint8_t* s_stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_off + El + 1) + 1023) & ~uintptr_t(1023));
     volatile int* abort = &st->abort;
@@ -155,6 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_addr(&st->tfull[b]), 1);
             ptx::mbar_init(ptx::smem_addr(&st->tempty[b]), kEpiWarps);
             ptx::mbar_init(ptx::smem_addr(&st->amax_bar[b]), kEpiWarps * 32);
+        }
+        for (int j = 0; j < kScaleRing; ++j) {
+            ptx::mbar_init(ptx::smem_addr(&st->sfull[j]), 32);  // one cp.async arrival per producer lane
+            ptx::mbar_init(ptx::smem_addr(&st->sempty[j]), kEpiWarps);
         }
         ptx::mbar_init(ptx::smem_addr(&st->mma_done), 1);
         st->abort = 0;
@@ -173,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the prologue above overlaps the previous kernel's end; global memory only after this
     pdl_wait();
     pdl_trigger();
-    for (int i = threadIdx.x; i <= El; i += kThreads) s_off[i] = __ldg(offsets + i);
+    for (int i = threadIdx.x; i <= El; i += threads_of<EPI>()) s_off[i] = __ldg(offsets + i);
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = st->tmem_base;
@@ -217,6 +254,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t j = first; j < it; ++j)
                 wait_phase(ptx::smem_addr(&st->full[j % C::kStages]), (j / C::kStages) & 1, abort, false);
         }
+    } else if (kStaged && warp == kScaleWarp) {
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+            const int mt = tile / n_tiles, nt = tile % n_tiles;
+            const int row0 = mt * kBM;
+            const int l = expert_of(s_off, El, row0);
+            // this lane's four rows of a_scale, and the tile's two W-scale rows
+            const float* sa_lane = sa + (int64_t)(row0 + lane) * KB;
+            const int nb0 = BN == 256 ? 2 * nt : nt;
+            const int nb1 = BN == 256 ? 2 * nt + 1 : nt;
+            const float* swa = sw + ((int64_t)l * NB + nb0) * KB;
+            const float* swb = sw + ((int64_t)l * NB + nb1) * KB;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int j = it % kScaleRing;
+                bool go = true;
+                if (lane == 0) go = wait_phase(ptx::smem_addr(&st->sempty[j]), ((it / kScaleRing) & 1) ^ 1, abort);
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) { ok = false; break; }
+                const uint32_t slot = ptx::smem_addr(&s_scale[j]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    ptx::cp_async4(slot + 4u * (uint32_t)(lane + 32 * q), sa_lane + (int64_t)32 * q * KB + kb);
+                if (lane == 0) {
+                    ptx::cp_async4(slot + 4u * kBM, swa + kb);
+                    ptx::cp_async4(slot + 4u * (kBM + 1), swb + kb);
+                }
+                ptx::cp_async_mbar_arrive_noinc(ptx::smem_addr(&st->sfull[j]));
+            }
+        }
+        // never leave with copies in flight
+        ptx::cp_async_wait_all();
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kBM, BN);
@@ -257,33 +326,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++tcount) {
             const int mt = tile / n_tiles, nt = tile % n_tiles;
             const int row0 = mt * kBM;
-            const int l = expert_of(s_off, El, row0);
             const int64_t r = row0 + row_in_tile;
             // fp32 accumulators as pairs, updated with packed fp32 FMAs (two per
             // instruction, each rounded exactly like fmaf)
             float2 acc2[C::kCols / 2];
 #pragma unroll
             for (int c = 0; c < C::kCols / 2; ++c) acc2[c] = make_float2(0.f, 0.f);
-            // block scales of this tile, fetched one K block ahead of their use
-            const float* sa_row = sa + r * KB;
-            const float* sw0 = sw + ((int64_t)l * NB + (kSilu ? nt : (BN == 256 ? nt * 2 + wg : nt))) * KB;
-            const float* sw1 = kSilu ? sw + ((int64_t)l * NB + NB / 2 + nt) * KB : sw0;
-            float sr_n = __ldg(sa_row), s0_n = __ldg(sw0), s1_n = kSilu ? __ldg(sw1) : s0_n;
             const uint32_t tcol = lane_field + (uint32_t)(wg * C::kCols);
+            // SiLU: this row's a_scale and the gate/up W scales, loaded one K block ahead
+            const float* sa_row = nullptr;
+            const float* sw0 = nullptr;
+            const float* sw1 = nullptr;
+            float sr_n = 0.f, s0_n = 0.f, s1_n = 0.f;
+            if constexpr (!kStaged) {
+                const int l = expert_of(s_off, El, row0);
+                sa_row = sa + r * KB;
+                sw0 = sw + ((int64_t)l * NB + nt) * KB;
+                sw1 = sw + ((int64_t)l * NB + NB / 2 + nt) * KB;
+                sr_n = __ldg(sa_row);
+                s0_n = __ldg(sw0);
+                s1_n = __ldg(sw1);
+            }
             for (int kb = 0; kb < KB; ++kb, ++it) {
-                const float sr = sr_n, sb0 = s0_n, sb1 = s1_n;
-                if (kb + 1 < KB) {
-                    sr_n = __ldg(sa_row + kb + 1);
-                    s0_n = __ldg(sw0 + kb + 1);
-                    if (kSilu) s1_n = __ldg(sw1 + kb + 1);
-                }
                 const int b = it & 1;
-                const uint32_t tph = (it >> 1) & 1;
-                bool got = wait_phase(ptx::smem_addr(&st->tfull[b]), tph, abort);
-                got = __all_sync(0xffffffffu, got);
-                if (!got) { ok = false; break; }
-                ptx::tc_fence_after();
-                const float s0 = sr * sb0, s1 = kSilu ? sr * sb1 : s0;
+                float s0, s1;  // scale products for the two halves of this thread's columns
+                if constexpr (kStaged) {
+                    // the K block's scales, staged by the scale warp well ahead
+                    const int j = it % kScaleRing;
+                    bool got = wait_phase(ptx::smem_addr(&st->sfull[j]), (it / kScaleRing) & 1, abort) &&
+                               wait_phase(ptx::smem_addr(&st->tfull[b]), (it >> 1) & 1, abort);
+                    got = __all_sync(0xffffffffu, got);
+                    if (!got) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    s0 = s1 = s_scale[j].sa[row_in_tile] * s_scale[j].sw[BN == 256 ? wg : 0];
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&st->sempty[j]));
+                } else {
+                    const float sr = sr_n, sb0 = s0_n, sb1 = s1_n;
+                    if (kb + 1 < KB) {
+                        sr_n = __ldg(sa_row + kb + 1);
+                        s0_n = __ldg(sw0 + kb + 1);
+                        s1_n = __ldg(sw1 + kb + 1);
+                    }
+                    bool got = wait_phase(ptx::smem_addr(&st->tfull[b]), (it >> 1) & 1, abort);
+                    got = __all_sync(0xffffffffu, got);
+                    if (!got) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    s0 = sr * sb0;
+                    s1 = sr * sb1;
+                }
                 const uint32_t tbase = tmem + tcol + (uint32_t)(b * BN);
                 // 16-column TMEM loads, double-buffered: the load of the next 16 columns
                 // is in flight while the current 16 are folded in
@@ -354,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            (uint32_t(f32x2_to_e4m3x2(acc[4 * q + 2], acc[4 * q + 3])) << 16);
                 const uint4 v4[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
                                      make_uint4(w[8], w[9], w[10], w[11]), make_uint4(w[12], w[13], w[14], w[15])};
-                store_box64(s_stage + warp * kStageWarpBytes, lane, v4, &tmO, nt * 128 + wg * 64, (int)(r - lane));
+                store_box64(s_stage + warp * C::kStageWarpBytes, lane, v4, &tmO, nt * 128 + wg * 64, (int)(r - lane));
                 if (wg == 0) out_scale[r * (N / 128) + nt] = s;
             } else if (EPI == MOE_EPI_F32) {
                 // 16 fp32 columns (64 bytes) per round
@@ -366,25 +457,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         v4[c] = make_uint4(__float_as_uint(acc[16 * q + 4 * c]), __float_as_uint(acc[16 * q + 4 * c + 1]),
                                            __float_as_uint(acc[16 * q + 4 * c + 2]),
                                            __float_as_uint(acc[16 * q + 4 * c + 3]));
-                    store_box64(s_stage + warp * kStageWarpBytes, lane, v4, &tmO, nt * BN + wg * C::kCols + q * 16,
+                    store_box64(s_stage + warp * C::kStageWarpBytes, lane, v4, &tmO, nt * BN + wg * C::kCols + q * 16,
                                 (int)(r - lane));
                 }
             } else {
-                // 32 bf16 columns (64 bytes) per round
+                // the warp's 32 rows x kCols bf16 columns as 128-byte-wide boxes (64
+                // columns each), written in TMA's 128-byte swizzle: 16-byte chunk c of row
+                // r sits at r * 128 + ((c ^ (r % 8)) * 16), so every 8 lanes of a store
+                // cover all 32 banks
+                uint8_t* stg = s_stage + warp * C::kStageWarpBytes;
+                if (lane == 0) ptx::bulk_wait_read0();  // the previous tile's stores have read it
+                __syncwarp();
 #pragma unroll
-                for (int q = 0; q < C::kCols / 32; ++q) {
-                    uint4 v4[4];
+                for (int q = 0; q < C::kCols / 64; ++q) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 8; ++c) {
                         uint32_t w[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = uint32_t(f32_to_bf16_bits(acc[32 * q + 8 * c + 2 * e])) |
-                                   (uint32_t(f32_to_bf16_bits(acc[32 * q + 8 * c + 2 * e + 1])) << 16);
-                        v4[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int e = 0; e < 4; ++e) {  // two round-to-nearest-even conversions per instruction
+                            __nv_bfloat162 h2 =
+                                __floats2bfloat162_rn(acc[64 * q + 8 * c + 2 * e], acc[64 * q + 8 * c + 2 * e + 1]);
+                            w[e] = *reinterpret_cast<uint32_t*>(&h2);
+                        }
+                        *reinterpret_cast<uint4*>(stg + q * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    store_box64(s_stage + warp * kStageWarpBytes, lane, v4, &tmO, nt * BN + wg * C::kCols + q * 32,
-                                (int)(r - lane));
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int q = 0; q < C::kCols / 64; ++q)
+                        ptx::tma_store_2d(&tmO, ptx::smem_addr(stg + q * 4096), nt * BN + wg * C::kCols + q * 64,
+                                          (int)(r - lane));
+                    ptx::bulk_commit();
                 }
             }
         }
@@ -426,8 +532,8 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Output tensor [rows, cols] of `esize`-byte elements, stored in boxes of 32 rows x 64
-// bytes with 64-byte swizzling (the epilogue's staging layout).
+// Output tensor [rows, cols] of `esize`-byte elements. Output map: bf16 in 32-row x 128-byte boxes with the 128-byte swizzle, fp8 and fp32
+// in 32-row x 64-byte boxes with the 64-byte swizzle (the staging layouts above).
 bool make_out_tmap(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, int esize) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -436,10 +542,12 @@ bool make_out_tmap(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, int
                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * (uint64_t)esize};
-    const cuuint32_t box[2] = {(cuuint32_t)(kStageRowBytes / esize), 32};
+    const bool wide = esize == 2;
+    const cuuint32_t box[2] = {(cuuint32_t)((wide ? 128 : kStageRowBytes) / esize), 32};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, int EPI>
@@ -447,19 +555,19 @@ int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& t
               const float* w_scale,
               const int32_t* offsets, int El, int64_t rp_cap, int n_out, int k_in, void* out, float* out_scale,
               int num_sms, cudaStream_t stream) {
-    const size_t smem = smem_bytes<BN>(El);
+    const size_t smem = smem_bytes<BN, EPI>(El);
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)smem_bytes<BN>(kMaxLocalExperts));
+                                        (int)smem_bytes<BN, EPI>(kMaxLocalExperts));
     });
     if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
     const int n_tiles = EPI == MOE_EPI_SILU_MUL_QUANT ? n_out / 256 : n_out / BN;
     const int64_t max_tiles = rp_cap / kBM * n_tiles;
     const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid < 1) return MOE_OK;
-    launch_k(gemm_tc_kernel<BN, EPI>, grid, kThreads, smem, stream, ta, tb, to, a_scale, w_scale, offsets, El, n_out, k_in, out, out_scale);
+    launch_k(gemm_tc_kernel<BN, EPI>, grid, threads_of<EPI>(), smem, stream, ta, tb, to, a_scale, w_scale, offsets, El, n_out, k_in, out, out_scale);
     note_launches(1);
     return launch_status();
 }
