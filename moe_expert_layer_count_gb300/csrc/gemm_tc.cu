@@ -23,10 +23,12 @@
 //  * Epilogues: bf16 or fp32 rows, or SiLU-and-mul with 1x128 FP8 requantisation. For
 //    the latter the W tile is gate rows [j, j+64) | up rows [j, j+64) | gate [j+64, j+128)
 //    | up [j+64, j+128), so each warpgroup holds matching gate/up columns of 64 outputs
-//    and one amax exchange per row completes the 128-wide group.
+//    and one amax exchange per row (shared memory and a hardware named barrier over the
+//    8 epilogue warps) completes the 128-wide group.
 // Every wait on a pipeline barrier gives up after 2 s, sets a device error word and an
 // abort flag seen by all roles, waits (bounded) for its own copies and MMAs in flight,
-// and the CTA frees its TMEM and returns.
+// and the CTA frees its TMEM and returns. An epilogue warp that gives up arrives on the
+// named barrier of the tile it leaves, so the exchange never waits for it.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -88,7 +90,6 @@ struct __align__(8) Tail {
     uint64_t empty[8];
     uint64_t tfull[2];
     uint64_t tempty[2];
-    uint64_t amax_bar[2];
     uint64_t sfull[kScaleRing];
     uint64_t sempty[kScaleRing];
     uint64_t mma_done;
@@ -187,7 +188,6 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_addr(&st->tfull[b]), 1);
             ptx::mbar_init(ptx::smem_addr(&st->tempty[b]), kEpiWarps);
-            ptx::mbar_init(ptx::smem_addr(&st->amax_bar[b]), kEpiWarps * 32);
         }
         for (int j = 0; j < kScaleRing; ++j) {
             ptx::mbar_init(ptx::smem_addr(&st->sfull[j]), 32);  // one cp.async arrival per producer lane
@@ -405,7 +405,12 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&st->tempty[b]));
             }
-            if (!ok) break;
+            if (!ok) {
+                // a warp leaving mid-tile still counts in that tile's amax exchange, so
+                // that no other epilogue warp can be left waiting at its barrier
+                if constexpr (kSilu) asm volatile("bar.arrive 1, 256;" ::: "memory");
+                break;
+            }
             float* acc = reinterpret_cast<float*>(acc2);
             if (kSilu) {
                 // acc[0:64) gate, acc[64:128) up of h columns nt*128 + wg*64 + [0, 64)
@@ -418,11 +423,10 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                 }
                 float* xa = s_amax + (tcount & 1) * 256;
                 xa[wg * 128 + row_in_tile] = amax;
-                const uint32_t abar = ptx::smem_addr(&st->amax_bar[tcount & 1]);
-                ptx::mbar_arrive(abar);
-                bool got = wait_phase(abar, (tcount >> 1) & 1, abort);
-                got = __all_sync(0xffffffffu, got);
-                if (!got) { ok = false; break; }
+                // both warpgroups' row maxima: hardware barrier 1 over the 8 epilogue warps
+                // (threads 0-255). Every epilogue warp reaches it once per tile, or has
+                // arrived on it when it left the tile early.
+                asm volatile("bar.sync 1, 256;" ::: "memory");
                 amax = fmaxf(xa[row_in_tile], xa[128 + row_in_tile]);
                 const float s = __fdiv_rn(amax, 448.0f);
                 // code = e4m3(h / s) with the correctly rounded quotient; the branch is per
