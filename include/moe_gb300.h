@@ -17,7 +17,10 @@
  * Conventions shared by every entry point:
  *  - Every pointer argument is a DEVICE pointer unless stated otherwise, owned by the
  *    caller. The library never allocates, frees or synchronises: each call only
- *    enqueues kernels (and, where stated, a memset) on `stream` and returns.
+ *    enqueues kernels (and, where stated, a memset) on `stream` and returns. The one
+ *    exception is moe_forward_host, which also enqueues copies on two streams of its
+ *    own (created with a few events on its first call on a device, kept for the life of
+ *    the process).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).
  *  - Return value: MOE_OK, or an error code from the host-side checks (nothing is
  *    enqueued then), or MOE_ERR_CUDA if a launch failed.
@@ -53,6 +56,7 @@ extern "C" {
 #endif
 
 typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+typedef struct CUevent_st* moe_event_t;   /* same type as cudaEvent_t */
 
 enum moe_status {
     MOE_OK = 0,
@@ -227,6 +231,41 @@ MOE_API int moe_forward_chunked(const void* hidden_states, const int32_t* topk_i
                                 int64_t M, int K, int N, int topk, int64_t chunk_size,
                                 int apply_router_weight_on_input, void* out, void* workspace,
                                 size_t workspace_bytes, int32_t* err_count, moe_stream_t stream);
+
+/* Workspace bytes moe_forward_host needs for batches of up to M tokens: the layer's own
+ * workspace (moe_workspace_size for min(chunk_size, M)) followed by two staging slots,
+ * each a device copy of a batch's hidden_states, topk_ids, topk_weights and output.
+ * Returns 0 on bad arguments. */
+MOE_API size_t moe_host_workspace_size(int64_t M, int K, int N, int topk, int local_num_experts,
+                                       int64_t chunk_size);
+
+/* moe_forward_chunked with the batch in HOST memory: hidden_states_host bf16 [M, K],
+ * topk_ids_host int32 [M, topk], topk_weights_host fp32 [M, topk] and out_host bf16
+ * [M, K] are host pointers; they must be page-locked (cudaHostAlloc / pinned tensors)
+ * for the copies to run asynchronously. Weights, expert_map, err_count and workspace
+ * are device pointers as in moe_forward_chunked, and the result is the same, bit for
+ * bit. The call is asynchronous:
+ *   - the inputs are copied into one of the workspace's two staging slots on a copy
+ *     stream of the library's own, once that slot's previous output has been copied
+ *     out; successive calls alternate slots;
+ *   - the layer runs on `stream` after the inputs have landed;
+ *   - the output is copied to out_host on a second copy stream of the library's own.
+ * So a call's input copy overlaps the previous call's layer, and its output copy the
+ * next call's layer. out_host holds the result once `done` (a cudaEvent_t, or NULL) has
+ * completed, or once `stream` has passed a later moe_host_wait. The host buffers must
+ * stay untouched until then. `stream` itself is NOT ordered after the output copy.
+ * Calls that share a workspace must use the same `stream`.
+ * workspace >= moe_host_workspace_size(M, K, N, topk, El, chunk_size) bytes. */
+MOE_API int moe_forward_host(const void* hidden_states_host, const int32_t* topk_ids_host,
+                             const float* topk_weights_host, const uint8_t* w13, const float* w13_scale,
+                             const uint8_t* w2, const float* w2_scale, const int32_t* expert_map, int E,
+                             int local_num_experts, int64_t M, int K, int N, int topk, int64_t chunk_size,
+                             int apply_router_weight_on_input, void* out_host, void* workspace,
+                             size_t workspace_bytes, int32_t* err_count, moe_stream_t stream, moe_event_t done);
+
+/* Makes `stream` wait until every output copy moe_forward_host has enqueued on the
+ * current device so far has completed. */
+MOE_API int moe_host_wait(moe_stream_t stream);
 
 #ifdef __cplusplus
 }

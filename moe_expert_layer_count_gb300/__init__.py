@@ -67,6 +67,10 @@ SIGNATURES = {
     "moe_gather_weight_reduce": ([_p, _p, _p, _i64, _int, _int, _int, _p, _p], _int),
     "moe_forward_chunked": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
                              _p, _p, _sz, _p, _p], _int),
+    "moe_host_workspace_size": ([_i64, _int, _int, _int, _int, _i64], _sz),
+    "moe_forward_host": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
+                          _p, _p, _sz, _p, _p, _p], _int),
+    "moe_host_wait": ([_p], _int),
 }
 
 
@@ -266,3 +270,58 @@ def moe_forward_chunked(hidden_states, topk_ids, topk_weights, w13, w13_scale, w
         int(bool(apply_router_weight_on_input)), _ptr(out), _ptr(workspace), workspace.numel(),
         _ptr(err_count), _stream(stream)))
     return out
+
+
+def _hptr(t: torch.Tensor):
+    """Address of a page-locked, contiguous host tensor."""
+    if t.is_cuda:
+        raise ValueError("expected a host tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if not t.is_pinned():
+        raise ValueError("expected a pinned (page-locked) host tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _event(done):
+    if done is None:
+        return None
+    if done.cuda_event == 0:  # torch creates the CUDA event lazily, on its first record
+        done.record()
+    return ctypes.c_void_p(done.cuda_event)
+
+
+def moe_host_workspace_size(M: int, K: int, N: int, topk: int, local_num_experts: int, chunk_size: int) -> int:
+    return int(lib().moe_host_workspace_size(M, K, N, topk, local_num_experts, chunk_size))
+
+
+def moe_forward_host(hidden_states, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, E, expert_map=None,
+                     chunk_size=None, apply_router_weight_on_input=False, out=None, workspace=None, err_count=None,
+                     stream=None, done=None):
+    """The layer with the batch in pinned HOST memory (hidden_states, topk_ids,
+    topk_weights and out are pinned CPU tensors); asynchronous: `out` holds the result
+    once the torch.cuda.Event `done` has completed, or once the stream has passed a later
+    moe_host_wait()."""
+    _dt(hidden_states, torch.bfloat16, "hidden_states")
+    _dt(topk_ids, torch.int32, "topk_ids")
+    _dt(topk_weights, torch.float32, "topk_weights")
+    M, K = hidden_states.shape
+    El, N2, _ = w13.shape
+    topk = topk_ids.shape[1]
+    chunk = M if chunk_size is None else int(chunk_size)
+    if out is None:
+        out = torch.empty(M, K, dtype=torch.bfloat16).pin_memory()
+    if workspace is None:
+        workspace = torch.empty(max(1, moe_host_workspace_size(max(1, M), K, N2 // 2, topk, El, max(1, chunk))),
+                                dtype=torch.uint8, device=w13.device)
+    _check("moe_forward_host", lib().moe_forward_host(
+        _hptr(hidden_states), _hptr(topk_ids), _hptr(topk_weights), _ptr(w13), _ptr(w13_scale), _ptr(w2),
+        _ptr(w2_scale), _ptr(expert_map), E, El, M, K, N2 // 2, topk, max(1, chunk),
+        int(bool(apply_router_weight_on_input)), _hptr(out), _ptr(workspace), workspace.numel(),
+        _ptr(err_count), _stream(stream), _event(done)))
+    return out
+
+
+def moe_host_wait(stream=None):
+    """Orders `stream` after every output copy moe_forward_host has enqueued so far."""
+    _check("moe_host_wait", lib().moe_host_wait(_stream(stream)))

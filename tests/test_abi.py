@@ -68,3 +68,21 @@ def test_argument_checks_return_before_any_launch(L):
     # workspace too small
     assert L.moe_forward_chunked(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 4, 0, p,
                                  ws, 16, None, None) == 2
+
+
+def test_host_entry_point_checks(L):
+    import moe_expert_layer_count_gb300 as moe
+    # two staging slots (x, ids, weights, out) after the layer's own workspace
+    lay = moe.moe_workspace_size(128, 2048, 768, 8, 64)
+    slot = 128 * 2048 * 2 + 128 * 8 * 4 * 2 + 128 * 2048 * 2
+    assert moe.moe_host_workspace_size(128, 2048, 768, 8, 64, 128) >= lay + 2 * slot
+    assert moe.moe_host_workspace_size(128, 2000, 768, 8, 64, 128) == 0   # K not a multiple of 128
+    assert moe.moe_host_workspace_size(0, 2048, 768, 8, 64, 128) == 0
+    p = ctypes.c_void_p(16)
+    # refused on the host before any copy or launch
+    assert L.moe_forward_host(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 0, 4, 0, p, p, 1 << 30,
+                              None, None, None) == 1                                   # topk 0
+    assert L.moe_forward_host(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 4, 0, p, p, 16,
+                              None, None, None) == 2                                   # workspace too small
+    assert L.moe_forward_host(p, p, p, p, p, p, p, None, 8, 8, 0, 128, 128, 2, 4, 0, p, p, 16,
+                              None, None, None) == 0                                   # M = 0: no-op
