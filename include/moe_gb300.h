@@ -176,7 +176,13 @@ MOE_API int moe_scatter_noalloc(const void* hidden_states, int64_t M, int K, con
  *   out[r, j] = sum_kb a_scale[r, kb] * w_scale[l, j/128, kb] *
  *               sum_{k in block kb} A[r, k] * W[l, j, k]
  * for every row r in [expert_offsets[l], expert_offsets[l+1]) of every local expert l
- * (padding rows included; rows >= expert_offsets[El] are not touched).
+ * (rows >= expert_offsets[El] are not touched).
+ *   expert_num_tokens int32 [El] or NULL. When given, the rows of a block at or past
+ *            expert_offsets[l] + expert_num_tokens[l] are padding, and for small batches
+ *            (rp_cap below 256 rows per local expert, where most of each block is padding)
+ *            an aligned group of 32 rows of a 128-row tile holding only padding is
+ *            neither folded nor written: those output rows keep their old contents. In
+ *            every other case all rows are computed, padding included.
  *   a        e4m3 [rp_cap, k_in];  a_scale fp32 [rp_cap, k_in/128]
  *   w        e4m3 [El, n_out, k_in] (each expert's rows are K-contiguous)
  *   w_scale  fp32 [El, n_out/128, k_in/128]
@@ -187,8 +193,9 @@ MOE_API int moe_scatter_noalloc(const void* hidden_states, int64_t M, int K, con
  *            fp32 scales [rp_cap, N/128], computed from the fp32 accumulators.
  * n_out and k_in are multiples of 128 (n_out a multiple of 256 for SILU_MUL_QUANT). */
 MOE_API int moe_grouped_gemm_fp8(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
-                                 const int32_t* expert_offsets, int local_num_experts, int64_t rp_cap, int n_out,
-                                 int k_in, int epilogue, void* out, float* out_scale, moe_stream_t stream);
+                                 const int32_t* expert_offsets, const int32_t* expert_num_tokens,
+                                 int local_num_experts, int64_t rp_cap, int n_out, int k_in, int epilogue, void* out,
+                                 float* out_scale, moe_stream_t stream);
 
 /* SiLU-and-mul with 1x128 FP8 requantisation, standalone (the same arithmetic the
  * SILU_MUL_QUANT epilogue applies):

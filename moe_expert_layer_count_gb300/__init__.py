@@ -62,7 +62,7 @@ SIGNATURES = {
                      _i64, _p, _sz, _p], _int),
     "moe_scatter_noalloc": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _int, _p, _p, _p, _p, _i64,
                              _p], _int),
-    "moe_grouped_gemm_fp8": ([_p, _p, _p, _p, _p, _int, _i64, _int, _int, _int, _p, _p, _p], _int),
+    "moe_grouped_gemm_fp8": ([_p, _p, _p, _p, _p, _p, _int, _i64, _int, _int, _int, _p, _p, _p], _int),
     "moe_silu_mul_quant": ([_p, _p, _int, _i64, _int, _p, _p, _p], _int),
     "moe_gather_weight_reduce": ([_p, _p, _p, _i64, _int, _int, _int, _p, _p], _int),
     "moe_forward_chunked": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
@@ -198,8 +198,9 @@ def moe_scatter_noalloc(hidden_states, topk_ids, topk_weights, E, local_num_expe
 
 
 def moe_grouped_gemm_fp8(a, a_scale, w, w_scale, expert_offsets, epilogue=MOE_EPI_BF16, out=None,
-                         out_scale=None, stream=None):
-    """Block-scaled FP8 grouped GEMM over the permuted rows (see the C header)."""
+                         out_scale=None, stream=None, expert_num_tokens=None):
+    """Block-scaled FP8 grouped GEMM over the permuted rows (see the C header). With
+    expert_num_tokens, 32-row groups of padding rows are neither computed nor written."""
     _dt(a, torch.uint8, "a")
     _dt(w, torch.uint8, "w")
     rp_cap, k_in = a.shape
@@ -214,7 +215,8 @@ def moe_grouped_gemm_fp8(a, a_scale, w, w_scale, expert_offsets, epilogue=MOE_EP
     if out_scale is None and epilogue == MOE_EPI_SILU_MUL_QUANT:
         out_scale = torch.empty(rp_cap, n_out // 256, dtype=torch.float32, device=dev)
     _check("moe_grouped_gemm_fp8", lib().moe_grouped_gemm_fp8(
-        _ptr(a), _ptr(a_scale), _ptr(w), _ptr(w_scale), _ptr(expert_offsets), El, rp_cap, n_out, k_in,
+        _ptr(a), _ptr(a_scale), _ptr(w), _ptr(w_scale), _ptr(expert_offsets), _ptr(expert_num_tokens), El, rp_cap,
+        n_out, k_in,
         epilogue, _ptr(out), _ptr(out_scale), _stream(stream)))
     return (out, out_scale) if epilogue == MOE_EPI_SILU_MUL_QUANT else out
 

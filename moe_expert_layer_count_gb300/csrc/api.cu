@@ -156,8 +156,9 @@ MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32
 }
 
 MOE_API int moe_grouped_gemm_fp8(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
-                                 const int32_t* expert_offsets, int local_num_experts, int64_t rp_cap, int n_out,
-                                 int k_in, int epilogue, void* out, float* out_scale, moe_stream_t stream) {
+                                 const int32_t* expert_offsets, const int32_t* expert_num_tokens,
+                                 int local_num_experts, int64_t rp_cap, int n_out, int k_in, int epilogue, void* out,
+                                 float* out_scale, moe_stream_t stream) {
     if (!a || !a_scale || !w || !w_scale || !expert_offsets || !out || local_num_experts < 1 ||
         local_num_experts > kMaxLocalExperts || rp_cap < 0 || rp_cap % kGroup || n_out <= 0 || k_in <= 0 ||
         n_out % kGroup || k_in % kGroup)
@@ -169,8 +170,8 @@ MOE_API int moe_grouped_gemm_fp8(const uint8_t* a, const float* a_scale, const u
         return MOE_ERR_INVALID_ARG;
     int sms = 0;
     if (int st = check_device(&sms)) return st;
-    return launch_grouped_gemm(a, a_scale, w, w_scale, expert_offsets, local_num_experts, rp_cap, n_out, k_in, epilogue,
-                               out, out_scale, sms, (cudaStream_t)stream);
+    return launch_grouped_gemm(a, a_scale, w, w_scale, expert_offsets, expert_num_tokens, local_num_experts, rp_cap,
+                               n_out, k_in, epilogue, out, out_scale, sms, (cudaStream_t)stream);
 }
 
 MOE_API int moe_silu_mul_quant(const float* c1, const int32_t* expert_offsets, int local_num_experts, int64_t rp_cap,
@@ -244,9 +245,10 @@ MOE_API int moe_forward_chunked(const void* hidden_states, const int32_t* topk_i
         int st = launch_scatter(x + c0 * K, Mc, K, ids, tw, topk, expert_map, E, El, nullptr, counts, err_count,
                                 apply_router_weight_on_input ? 1 : 0, MOE_QUANT_FP8_1X128, A, sa, offs, s2d, hist, s);
         if (!st)
-            st = launch_grouped_gemm(A, sa, w13, w13_scale, offs, El, cap, 2 * N, K, MOE_EPI_SILU_MUL_QUANT, H, sh,
+            st = launch_grouped_gemm(A, sa, w13, w13_scale, offs, counts, El, cap, 2 * N, K, MOE_EPI_SILU_MUL_QUANT, H, sh,
                                      sms, s);
-        if (!st) st = launch_grouped_gemm(H, sh, w2, w2_scale, offs, El, cap, K, N, MOE_EPI_BF16, Y, nullptr, sms, s);
+        if (!st)
+            st = launch_grouped_gemm(H, sh, w2, w2_scale, offs, counts, El, cap, K, N, MOE_EPI_BF16, Y, nullptr, sms, s);
         if (!st) st = launch_gather(Y, s2d, tw, Mc, topk, K, apply_router_weight_on_input ? 1 : 0, o + c0 * K, s);
         if (st) return st;
     }

@@ -103,7 +103,7 @@ template <int BN, int EPI>
 constexpr size_t smem_bytes(int El) {
     using C = Cfg<BN, EPI>;
     return 1024 + (size_t)C::kStages * C::kStageBytes + sizeof(Tail) + 16 + kScaleRing * sizeof(ScaleSlot) +
-           2 * 2 * 128 * sizeof(float) + (size_t)(El + 1) * sizeof(int32_t) + 1024 +
+           2 * 2 * 128 * sizeof(float) + (size_t)(2 * El + 1) * sizeof(int32_t) + 1024 +
            (size_t)kEpiWarps * C::kStageWarpBytes;
 }
 
@@ -161,10 +161,11 @@ __device__ __forceinline__ int expert_of(const int32_t* s_off, int El, int row0)
 }
 
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool kSkip>
 __global__ void __launch_bounds__(threads_of<EPI>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmO, const float* __restrict__ sa, const float* __restrict__ sw, const int32_t* __restrict__ offsets,
+                   const __grid_constant__ CUtensorMap tmO, const float* __restrict__ sa, const float* __restrict__ sw,
+                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts,
                    int El, int n_out, int k_in, void* __restrict__ out, float* __restrict__ out_scale) {
     using C = Cfg<BN, EPI>;
     constexpr bool kSilu = EPI == MOE_EPI_SILU_MUL_QUANT;
@@ -176,7 +177,9 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
     ScaleSlot* s_scale = reinterpret_cast<ScaleSlot*>((reinterpret_cast<uintptr_t>(st + 1) + 15) & ~uintptr_t(15));
     float* s_amax = reinterpret_cast<float*>(s_scale + kScaleRing);  // [2 parities][2 warpgroups][128 rows]
     int32_t* s_off = reinterpret_cast<int32_t*>(s_amax + 2 * 2 * 128);
-    uint8_t* s_stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_off + El + 1) + 1023) & ~uintptr_t(1023));
+    int32_t* s_cnt = s_off + El + 1;  // valid rows of each expert's block (kSkip only)
+    uint8_t* s_stage = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(s_cnt + (kSkip ? El : 0)) + 1023) & ~uintptr_t(1023));
     volatile int* abort = &st->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -210,7 +213,10 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
     // the prologue above overlaps the previous kernel's end; global memory only after this
     pdl_wait();
     pdl_trigger();
-    for (int i = threadIdx.x; i <= El; i += threads_of<EPI>()) s_off[i] = __ldg(offsets + i);
+    for (int i = threadIdx.x; i <= El; i += threads_of<EPI>()) {
+        s_off[i] = __ldg(offsets + i);
+        if (kSkip && i < El) s_cnt[i] = __ldg(counts + i);
+    }
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = st->tmem_base;
@@ -327,6 +333,42 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
             const int mt = tile / n_tiles, nt = tile % n_tiles;
             const int row0 = mt * kBM;
             const int64_t r = row0 + row_in_tile;
+            if constexpr (kSkip) {
+                // a warp whose 32 rows are all padding of the expert's block (small
+                // batches leave most of a block empty) reads no partial sums and stores
+                // nothing: it only keeps step with the pipeline barriers
+                const int le = expert_of(s_off, El, row0);
+                if ((warp & 3) * 32 >= s_off[le] + s_cnt[le] - row0) {
+                    for (int kb = 0; kb < KB; ++kb, ++it) {
+                        const int b = it & 1;
+                        bool got;
+                        if constexpr (kStaged) {
+                            const int j = it % kScaleRing;
+                            got = wait_phase(ptx::smem_addr(&st->sfull[j]), (it / kScaleRing) & 1, abort) &&
+                                  wait_phase(ptx::smem_addr(&st->tfull[b]), (it >> 1) & 1, abort);
+                        } else {
+                            got = wait_phase(ptx::smem_addr(&st->tfull[b]), (it >> 1) & 1, abort);
+                        }
+                        got = __all_sync(0xffffffffu, got);
+                        if (!got) { ok = false; break; }
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (kStaged) ptx::mbar_arrive(ptx::smem_addr(&st->sempty[it % kScaleRing]));
+                            ptx::mbar_arrive(ptx::smem_addr(&st->tempty[b]));
+                        }
+                    }
+                    if (kSilu) {
+                        if (!ok) {
+                            asm volatile("bar.arrive 1, 256;" ::: "memory");
+                            break;
+                        }
+                        // the partner warp (same rows) is idle too; the exchange still
+                        // needs every epilogue warp once per tile
+                        asm volatile("bar.sync 1, 256;" ::: "memory");
+                    }
+                    continue;
+                }
+            }
             // fp32 accumulators as pairs, updated with packed fp32 FMAs (two per
             // instruction, each rounded exactly like fmaf)
             float2 acc2[C::kCols / 2];
@@ -554,16 +596,15 @@ bool make_out_tmap(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI>
-int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const float* a_scale,
-              const float* w_scale,
-              const int32_t* offsets, int El, int64_t rp_cap, int n_out, int k_in, void* out, float* out_scale,
-              int num_sms, cudaStream_t stream) {
+template <int BN, int EPI, bool kSkip>
+int launch_tc_k(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const float* a_scale,
+                const float* w_scale, const int32_t* offsets, const int32_t* counts, int El, int64_t rp_cap,
+                int n_out, int k_in, void* out, float* out_scale, int num_sms, cudaStream_t stream) {
     const size_t smem = smem_bytes<BN, EPI>(El);
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, kSkip>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)smem_bytes<BN, EPI>(kMaxLocalExperts));
     });
     if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
@@ -571,15 +612,31 @@ int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& t
     const int64_t max_tiles = rp_cap / kBM * n_tiles;
     const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid < 1) return MOE_OK;
-    launch_k(gemm_tc_kernel<BN, EPI>, grid, threads_of<EPI>(), smem, stream, ta, tb, to, a_scale, w_scale, offsets, El, n_out, k_in, out, out_scale);
+    launch_k(gemm_tc_kernel<BN, EPI, kSkip>, grid, threads_of<EPI>(), smem, stream, ta, tb, to, a_scale, w_scale,
+             offsets, counts, El, n_out, k_in, out, out_scale);
     note_launches(1);
     return launch_status();
+}
+
+// Small batches (fewer than two 128-row blocks per local expert on average, so that most
+// of each block is padding) run the kernel that skips all-padding row groups; large ones
+// the kernel without that path, which leaves its registers to the full tiles.
+template <int BN, int EPI>
+int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const float* a_scale,
+              const float* w_scale, const int32_t* offsets, const int32_t* counts, int El, int64_t rp_cap, int n_out,
+              int k_in, void* out, float* out_scale, int num_sms, cudaStream_t stream) {
+    if (counts && rp_cap < (int64_t)El * 2 * kBM)
+        return launch_tc_k<BN, EPI, true>(ta, tb, to, a_scale, w_scale, offsets, counts, El, rp_cap, n_out, k_in, out,
+                                          out_scale, num_sms, stream);
+    return launch_tc_k<BN, EPI, false>(ta, tb, to, a_scale, w_scale, offsets, counts, El, rp_cap, n_out, k_in, out,
+                                       out_scale, num_sms, stream);
 }
 
 }  // namespace
 
 int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
-                        const int32_t* expert_offsets, int El, int64_t rp_cap, int n_out, int k_in, int epilogue,
+                        const int32_t* expert_offsets, const int32_t* expert_counts, int El, int64_t rp_cap, int n_out,
+                        int k_in, int epilogue,
                         void* out, float* out_scale, int num_sms, cudaStream_t stream) {
     if (rp_cap == 0) return MOE_OK;
     const bool bn256 = n_out % 256 == 0;
@@ -592,17 +649,17 @@ int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w
         return MOE_ERR_CUDA;
     switch (epilogue) {
         case MOE_EPI_SILU_MUL_QUANT:
-            return launch_tc<256, MOE_EPI_SILU_MUL_QUANT>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+            return launch_tc<256, MOE_EPI_SILU_MUL_QUANT>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                           k_in, out, out_scale, num_sms, stream);
         case MOE_EPI_F32:
-            return bn256 ? launch_tc<256, MOE_EPI_F32>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+            return bn256 ? launch_tc<256, MOE_EPI_F32>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                        k_in, out, out_scale, num_sms, stream)
-                         : launch_tc<128, MOE_EPI_F32>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+                         : launch_tc<128, MOE_EPI_F32>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                        k_in, out, out_scale, num_sms, stream);
         default:
-            return bn256 ? launch_tc<256, MOE_EPI_BF16>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+            return bn256 ? launch_tc<256, MOE_EPI_BF16>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                         k_in, out, out_scale, num_sms, stream)
-                         : launch_tc<128, MOE_EPI_BF16>(ta, tb, to, a_scale, w_scale, expert_offsets, El, rp_cap, n_out,
+                         : launch_tc<128, MOE_EPI_BF16>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                         k_in, out, out_scale, num_sms, stream);
     }
 }

@@ -29,9 +29,12 @@ int launch_gather(const uint16_t* y, const int32_t* src2dst, const float* topk_w
 int launch_silu_mul_quant(const float* c1, const int32_t* expert_offsets, int El, int64_t rp_cap, int N, uint8_t* h,
                           float* h_scale, cudaStream_t stream);
 
+// expert_counts (nullable): valid rows of each expert's block; rows past them are
+// padding, and 32-row groups made only of padding are neither computed nor stored.
 int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
-                        const int32_t* expert_offsets, int El, int64_t rp_cap, int n_out, int k_in, int epilogue,
-                        void* out, float* out_scale, int num_sms, cudaStream_t stream);
+                        const int32_t* expert_offsets, const int32_t* expert_counts, int El, int64_t rp_cap,
+                        int n_out, int k_in, int epilogue, void* out, float* out_scale, int num_sms,
+                        cudaStream_t stream);
 
 // Device error word of the grouped GEMM (1: a pipeline wait ran out of time). Reading
 // it synchronises the device; `clear` resets it.

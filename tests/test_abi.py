@@ -59,7 +59,7 @@ def test_argument_checks_return_before_any_launch(L):
     assert L.moe_count_expert_tokens(p, 4, 2, None, 8, 0, p, None, None) == 1          # El 0
     assert L.moe_count_expert_tokens(p, 4, 2, None, 8, 2000, p, None, None) == 1       # El > 1024
     assert L.moe_gather_weight_reduce(p, p, p, 4, 2, 100, 0, p, None) == 1             # K % 128
-    assert L.moe_grouped_gemm_fp8(p, p, p, p, p, 4, 128, 384, 256, 2, p, p, None) == 1  # silu needs n_out%256
+    assert L.moe_grouped_gemm_fp8(p, p, p, p, p, None, 4, 128, 384, 256, 2, p, p, None) == 1  # silu: n_out%256
     assert L.moe_silu_mul_quant(None, p, 4, 128, 128, p, p, None) == 1
     ws = ctypes.c_void_p(4096)
     # out overlapping the workspace is refused

@@ -77,6 +77,39 @@ def test_grouped_gemm_silu_epilogue(counts, N, K):
     assert d.max() <= 1 and (d == 0).mean() >= 0.99
 
 
+@pytest.mark.parametrize("epi", [moe.MOE_EPI_SILU_MUL_QUANT, moe.MOE_EPI_BF16, moe.MOE_EPI_F32])
+def test_grouped_gemm_with_counts_skips_padding(epi):
+    """With expert_num_tokens the kept rows are bit-identical to the run without it, and
+    aligned 32-row groups of pure padding are left untouched (their sentinel survives)."""
+    counts = [1, 33, 0, 64, 100, 130]
+    K, n_out = 384, 512
+    counts, offs, A, SA = permuted_inputs(counts, K, seed=5)
+    El = len(counts)
+    W, S = mi.expert_weights(El, n_out, K, seed=8, stream=1)
+    a, sa, w, s, o = dev(A), dev(SA), dev(W), dev(S), dev(offs)
+    full = moe.moe_grouped_gemm_fp8(a, sa, w, s, o, epi)
+    torch.cuda.synchronize()
+    R = A.shape[0]
+    cols = n_out // 2 if epi == moe.MOE_EPI_SILU_MUL_QUANT else n_out
+    dt = {moe.MOE_EPI_SILU_MUL_QUANT: torch.uint8, moe.MOE_EPI_BF16: torch.bfloat16, moe.MOE_EPI_F32: torch.float32}
+    out = torch.full((R, cols), 7, dtype=dt[epi], device="cuda")
+    osc = torch.full((R, n_out // 256), -1.0, device="cuda") if epi == moe.MOE_EPI_SILU_MUL_QUANT else None
+    got = moe.moe_grouped_gemm_fp8(a, sa, w, s, o, epi, out=out, out_scale=osc, expert_num_tokens=dev(counts))
+    torch.cuda.synchronize()
+    rows = kept_rows(offs, counts)
+    g, f = (got[0], full[0]) if epi == moe.MOE_EPI_SILU_MUL_QUANT else (got, full)
+    assert torch.equal(g[rows].view(torch.uint8), f[rows].view(torch.uint8))
+    if epi == moe.MOE_EPI_SILU_MUL_QUANT:
+        assert torch.equal(got[1][rows], full[1][rows])
+    # rows of 32-row groups that hold no kept row keep the sentinel
+    idle = [r for l in range(El) for r in range(int(offs[l]), int(offs[l + 1]))
+            if (r - int(offs[l])) // 32 * 32 >= counts[l]]
+    assert idle, "the case must have idle groups"
+    assert bool((g[idle] == 7).all())
+    if epi == moe.MOE_EPI_SILU_MUL_QUANT:
+        assert bool((got[1][idle] == -1).all())
+
+
 def test_device_error_word_is_clear():
     assert moe.moe_device_error() == 0
 
