@@ -103,7 +103,7 @@ int launch_count(const int32_t* ids, int64_t n, const int32_t* expert_map, int E
 constexpr int kRound = 8;  // groups of 32 slots loaded per warp per round
 
 int scatter_slots_per_cta(int64_t n) {
-    constexpr int64_t kUnit = (kScatterThreads / 32) * 32 * kRound;  // 2048: one round for each warp
+    constexpr int64_t kUnit = (kScatterThreads / 32) * 32;  // 32 slots for each warp
     int64_t per = (n + kMaxScatterCtas - 1) / kMaxScatterCtas;
     per = (per + kUnit - 1) / kUnit * kUnit;
     return (int)(per < kScatterMinSlots ? kScatterMinSlots : per);

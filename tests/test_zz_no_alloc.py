@@ -80,7 +80,7 @@ def test_noalloc_scatter_matches_scatter_on_two_calls():
 
 
 def test_noalloc_scatter_refuses_problems_beyond_its_scratch():
-    # 1024 local experts x 79 scatter blocks (160000 slots) > 65536 entries: refused on
+    # 1024 local experts x 157 scatter blocks (160000 slots) > 65536 entries: refused on
     # the host with MOE_ERR_SCRATCH_LIMIT, nothing enqueued
     p = ctypes.c_void_p(256)
     st = moe.lib().moe_scatter_noalloc(p, 20000, 128, p, p, 8, None, 1024, 1024, p, 0, 1, p, p, p, p,
