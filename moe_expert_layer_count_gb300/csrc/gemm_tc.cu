@@ -64,7 +64,8 @@ struct Cfg {
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = BN * kBK;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kTmemBufs = 512 / BN;  // K-block partials TMEM holds at once
+    static constexpr int kTmemCols = kTmemBufs * BN;
     static constexpr int kCols = BN / 2;  // accumulator columns per epilogue thread
     // bf16 output leaves in 128-byte-wide boxes from a staging buffer that holds the
     // warp's whole 32-row slab (all its stores of a tile go out without waiting); the
@@ -88,8 +89,8 @@ constexpr int kScaleRing = 8;
 struct __align__(8) Tail {
     uint64_t full[8];
     uint64_t empty[8];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t tfull[4];
+    uint64_t tempty[4];
     uint64_t sfull[kScaleRing];
     uint64_t sempty[kScaleRing];
     uint64_t mma_done;
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
             ptx::mbar_init(ptx::smem_addr(&st->full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&st->empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kTmemBufs; ++b) {
             ptx::mbar_init(ptx::smem_addr(&st->tfull[b]), 1);
             ptx::mbar_init(ptx::smem_addr(&st->tempty[b]), kEpiWarps);
         }
@@ -301,8 +302,8 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % C::kStages;
                     const uint32_t ph = (it / C::kStages) & 1;
-                    const int b = it & 1;
-                    const uint32_t tph = (it >> 1) & 1;
+                    const int b = it % C::kTmemBufs;
+                    const uint32_t tph = (it / C::kTmemBufs) & 1;
                     if (!wait_phase(ptx::smem_addr(&st->tempty[b]), tph ^ 1, abort)) { ok = false; break; }
                     if (!wait_phase(ptx::smem_addr(&st->full[s]), ph, abort)) { ok = false; break; }
                     ptx::tc_fence_after();
@@ -340,14 +341,14 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                 const int le = expert_of(s_off, El, row0);
                 if ((warp & 3) * 32 >= s_off[le] + s_cnt[le] - row0) {
                     for (int kb = 0; kb < KB; ++kb, ++it) {
-                        const int b = it & 1;
+                        const int b = it % C::kTmemBufs;
                         bool got;
                         if constexpr (kStaged) {
                             const int j = it % kScaleRing;
                             got = wait_phase(ptx::smem_addr(&st->sfull[j]), (it / kScaleRing) & 1, abort) &&
-                                  wait_phase(ptx::smem_addr(&st->tfull[b]), (it >> 1) & 1, abort);
+                                  wait_phase(ptx::smem_addr(&st->tfull[b]), (it / C::kTmemBufs) & 1, abort);
                         } else {
-                            got = wait_phase(ptx::smem_addr(&st->tfull[b]), (it >> 1) & 1, abort);
+                            got = wait_phase(ptx::smem_addr(&st->tfull[b]), (it / C::kTmemBufs) & 1, abort);
                         }
                         got = __all_sync(0xffffffffu, got);
                         if (!got) { ok = false; break; }
@@ -390,13 +391,13 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                 s1_n = __ldg(sw1);
             }
             for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int b = it & 1;
+                const int b = it % C::kTmemBufs;
                 float s0, s1;  // scale products for the two halves of this thread's columns
                 if constexpr (kStaged) {
                     // the K block's scales, staged by the scale warp well ahead
                     const int j = it % kScaleRing;
                     bool got = wait_phase(ptx::smem_addr(&st->sfull[j]), (it / kScaleRing) & 1, abort) &&
-                               wait_phase(ptx::smem_addr(&st->tfull[b]), (it >> 1) & 1, abort);
+                               wait_phase(ptx::smem_addr(&st->tfull[b]), (it / C::kTmemBufs) & 1, abort);
                     got = __all_sync(0xffffffffu, got);
                     if (!got) { ok = false; break; }
                     ptx::tc_fence_after();
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                         s0_n = __ldg(sw0 + kb + 1);
                         s1_n = __ldg(sw1 + kb + 1);
                     }
-                    bool got = wait_phase(ptx::smem_addr(&st->tfull[b]), (it >> 1) & 1, abort);
+                    bool got = wait_phase(ptx::smem_addr(&st->tfull[b]), (it / C::kTmemBufs) & 1, abort);
                     got = __all_sync(0xffffffffu, got);
                     if (!got) { ok = false; break; }
                     ptx::tc_fence_after();
