@@ -183,6 +183,10 @@ MOE_API int moe_scatter_noalloc(const void* hidden_states, int64_t M, int K, con
  *            an aligned group of 32 rows of a 128-row tile holding only padding is
  *            neither folded nor written: those output rows keep their old contents. In
  *            every other case all rows are computed, padding included.
+ *            The batched ("masked") expert layout [El, max_tokens, K] that low-latency
+ *            expert-parallel dispatch produces is the case expert_offsets[l] =
+ *            l * max_tokens (max_tokens a multiple of 128) with expert_num_tokens = the
+ *            per-expert token counts (the mask).
  *   a        e4m3 [rp_cap, k_in];  a_scale fp32 [rp_cap, k_in/128]
  *   w        e4m3 [El, n_out, k_in] (each expert's rows are K-contiguous)
  *   w_scale  fp32 [El, n_out/128, k_in/128]

@@ -110,6 +110,38 @@ def test_grouped_gemm_with_counts_skips_padding(epi):
         assert bool((got[1][idle] == -1).all())
 
 
+@pytest.mark.parametrize("epi", [moe.MOE_EPI_BF16, moe.MOE_EPI_SILU_MUL_QUANT])
+def test_grouped_gemm_masked_batched_layout(epi):
+    """The batched ("masked") expert layout [El, max_tokens, K] that low-latency
+    expert-parallel dispatch produces: expert l owns rows [l * max_tokens, (l+1) *
+    max_tokens) and only its first mask[l] rows hold tokens. It is the grouped GEMM with
+    expert_offsets = l * max_tokens and expert_num_tokens = mask."""
+    El, max_tokens, K = 8, 256, 384
+    n_out = 512
+    rng = np.random.default_rng(11)
+    mask = rng.integers(0, max_tokens + 1, El).astype(np.int32)
+    mask[2], mask[5] = 0, max_tokens
+    offs = (np.arange(El + 1) * max_tokens).astype(np.int32)
+    x = (rng.standard_normal((El * max_tokens, K)) * rng.uniform(0.05, 8, (El * max_tokens, 1))).astype(np.float32)
+    A, SA = oracle.quant_rows(x)
+    W, S = mi.expert_weights(El, n_out, K, seed=12, stream=1)
+    out = moe.moe_grouped_gemm_fp8(dev(A), dev(SA), dev(W), dev(S), dev(offs), epi, expert_num_tokens=dev(mask))
+    torch.cuda.synchronize()
+    rows = kept_rows(offs, mask)
+    C = oracle.grouped_gemm(A, SA, W, S, offs, mask)
+    if epi == moe.MOE_EPI_BF16:
+        got = mi.bf16_to_f32(host_bits(out)[rows]).astype(np.float64)
+        ref = C[rows]
+        assert np.abs(got - ref).max() <= 8e-3 * np.abs(ref).max()
+    else:
+        counts = mask
+        Href, hsref = oracle.silu_mul_quant(C.astype(np.float32), offs, counts)
+        hs = host(out[1])[rows]
+        np.testing.assert_allclose(hs, hsref[rows], rtol=2e-5, atol=0)
+        d = e4m3_ulp_diff(host(out[0])[rows], Href[rows])
+        assert d.max() <= 1 and (d == 0).mean() >= 0.99
+
+
 def test_device_error_word_is_clear():
     assert moe.moe_device_error() == 0
 
@@ -194,6 +226,20 @@ def test_layer_no_local_expert_is_zero(tiny):
     d2 = dict(d, m=dev(m))
     got = gpu_forward(d2, E)
     assert (mi.bf16_to_f32(got) == 0).all()
+
+
+@pytest.mark.parametrize("E,topk,local,chunk", [(1024, 8, None, None),   # the most local experts the ABI takes
+                                               (64, 1, None, 77),       # top-1, ragged chunks
+                                               (64, 32, 48, None),      # the widest top-k, a local subset
+                                               (1, 1, None, None)])     # a single expert
+def test_layer_interface_extremes(E, topk, local, chunk):
+    """The layer at the ends of its argument ranges, against the oracle."""
+    wl = mi.Workload(f"extreme_e{E}_top{topk}", M=300, K=256, N=256, E=E, topk=topk, seed=E + topk,
+                     zipf_s=1.2, local_experts=local, chunk_size=chunk)
+    li = mi.make_layer_inputs(wl)
+    got = gpu_forward(to_dev_layer(li), E, chunk=chunk)
+    ref = oracle_forward(li, chunk=chunk)
+    layer_tolerance(got, ref)
 
 
 @pytest.fixture(scope="module")
