@@ -13,7 +13,8 @@
 //    each epilogue thread loads its row's scales itself, one K block ahead (measured
 //    faster for that GEMM, whose 16 K blocks per tile leave the loads time to land);
 //  * warp 9 (one thread) issues tcgen05.mma kind::f8f6f4 (M=128, N=BN, K=32, four per
-//    K block) into one of two TMEM accumulators, starting each K block from zero;
+//    K block) into one of the 512/BN TMEM accumulators (two for 256-wide tiles),
+//    starting each K block from zero;
 //  * warps 0-7 (two warpgroups, each one TMEM lane = one row per thread, half of the
 //    tile's columns each) read the K block's partial sums from TMEM, release the buffer
 //    and fold them into fp32 registers with the product of the two block scales. The
@@ -25,6 +26,8 @@
 //    | up [j+64, j+128), so each warpgroup holds matching gate/up columns of 64 outputs
 //    and one amax exchange per row (shared memory and a hardware named barrier over the
 //    8 epilogue warps) completes the 128-wide group.
+// Small batches (given the experts' valid row counts) run a variant in which an epilogue
+// warp whose 32 rows are all padding skips the TMEM reads, folding and stores.
 // Every wait on a pipeline barrier gives up after 2 s, sets a device error word and an
 // abort flag seen by all roles, waits (bounded) for its own copies and MMAs in flight,
 // and the CTA frees its TMEM and returns. An epilogue warp that gives up arrives on the
