@@ -53,7 +53,7 @@ class Workload:
         return self.M if self.chunk_size is None else self.chunk_size
 
 
-# The five workloads of this build: a tiny layer, a permute/unpermute-only pass, and a
+# The five workloads: a tiny layer, a permute/unpermute-only pass, and a
 # Qwen3-30B-A3B-shaped layer (hidden 2048, moe intermediate 768, 128 experts, top-8)
 # at decode size, at prefill size with skewed routing, and chunked with half the
 # experts local.
