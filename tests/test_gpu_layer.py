@@ -242,6 +242,36 @@ def test_layer_interface_extremes(E, topk, local, chunk):
     layer_tolerance(got, ref)
 
 
+def random_layer_case(seed):
+    """A seeded random layer configuration: sizes, expert count, top-k, a random local
+    expert map (or none), chunking, routing skew and where the router weight applies."""
+    rng = np.random.default_rng(1000 + seed)
+    E = int(rng.choice([1, 3, 16, 64, 200]))
+    topk = int(rng.integers(1, min(E, 8) + 1))
+    wl = mi.Workload(f"random_{seed}", M=int(rng.integers(1, 700)), K=int(rng.choice([128, 256, 384])),
+                     N=int(rng.choice([128, 256, 384])), E=E, topk=topk, seed=2000 + seed,
+                     zipf_s=float(rng.choice([0.0, 1.2])),
+                     chunk_size=int(rng.choice([0, 1, 33, 128, 256])) or None,
+                     apply_router_weight_on_input=bool(rng.integers(0, 2)) and topk == 1)
+    li = mi.make_layer_inputs(wl)
+    if E > 1 and rng.integers(0, 2):
+        local = int(rng.integers(1, E + 1))
+        li.expert_map = mi.random_expert_map(E, local, seed=3000 + seed)
+        li.w13, li.w13_scale = mi.expert_weights(local, 2 * wl.N, wl.K, wl.seed, 13)
+        li.w2, li.w2_scale = mi.expert_weights(local, wl.K, wl.N, wl.seed, 2)
+    return li
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_layer_random_configurations(seed):
+    li = random_layer_case(seed)
+    wl = li.wl
+    apply = wl.apply_router_weight_on_input
+    got = gpu_forward(to_dev_layer(li), wl.E, chunk=wl.chunk_size, apply_on_input=apply)
+    ref = oracle_forward(li, chunk=wl.chunk_size, apply_on_input=apply)
+    layer_tolerance(got, ref)
+
+
 @pytest.fixture(scope="module")
 def decode():
     li = mi.make_layer_inputs(mi.QWEN3_DECODE)
