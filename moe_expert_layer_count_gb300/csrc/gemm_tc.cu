@@ -643,7 +643,12 @@ int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w
                         int k_in, int epilogue,
                         void* out, float* out_scale, int num_sms, cudaStream_t stream) {
     if (rp_cap == 0) return MOE_OK;
-    const bool bn256 = n_out % 256 == 0;
+    // 256-wide tiles, except for a bf16/fp32 output of a small batch whose 256-wide tiles
+    // would fill fewer than four waves of the SMs (a 128-token chunk: ~3 waves, the last
+    // mostly idle): twice as many 128-wide tiles balance the SMs better there
+    const bool small = expert_counts && rp_cap < (int64_t)El * 2 * kBM;
+    const bool few_tiles = rp_cap / kBM * (n_out / 256) < 4 * (int64_t)num_sms;
+    const bool bn256 = n_out % 256 == 0 && !(small && few_tiles && epilogue != MOE_EPI_SILU_MUL_QUANT);
     CUtensorMap ta, tb, to;
     const int o_cols = epilogue == MOE_EPI_SILU_MUL_QUANT ? n_out / 2 : n_out;
     const int o_esize = epilogue == MOE_EPI_SILU_MUL_QUANT ? 1 : epilogue == MOE_EPI_F32 ? 4 : 2;
