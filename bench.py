@@ -174,6 +174,88 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------ our arm
+def run_count_only(args, world, local_rank):
+    """The count step alone (count_expert_num_tokens) over 2^20 tokens of top-8 ids. The
+    ids (33.5 MB) fit in L2, so L2 is flushed (a 256 MB write) before every timed step and
+    each step is timed by its own events."""
+    import torch
+
+    import moe_expert_layer_count_gb300 as moe
+    moe.lib()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = mi.WORKLOADS[args.workload]
+    ids_np, _ = mi.route(wl.M, wl.E, wl.topk, wl.seed, wl.zipf_s)
+    ids = torch.from_numpy(ids_np).to(dev)
+    cnt = torch.empty(wl.El, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i_ids=ids):
+        moe.moe_count_expert_tokens(i_ids, wl.E, wl.El, None, expert_num_tokens=cnt, err_count=err)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    clk = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
+                       if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
+    clk.start()
+    clk.mark_on()
+    l0 = moe.moe_kernel_launch_count()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk.mark_off()
+    clk.stop()
+    launches = moe.moe_kernel_launch_count() - l0
+    ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs), world, dev)
+    nbytes = wl.M * wl.topk * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    pk = peaks()
+    # end to end: the ids copied in from pinned memory, the counts read back, every step
+    ih = torch.from_numpy(ids_np).pin_memory()
+    ch = torch.empty(wl.El, dtype=torch.int32).pin_memory()
+    for _ in range(3):
+        ids.copy_(ih, non_blocking=True)
+        step()
+        ch.copy_(cnt, non_blocking=True)
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        ids.copy_(ih, non_blocking=True)
+        step()
+        ch.copy_(cnt, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / n_e2e
+    return {
+        "metric": "MoE-layer tokens/s", "value": round(job_throughput(wl.M, world, ms), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic: seeded N(0,1) router logits, top-8 of 128 experts",
+        "config": {"workload": wl.name, "M": wl.M, "experts": wl.E, "topk": wl.topk, "step": "count only",
+                   "l2": "flushed before every timed step (256 MB write); each step timed by its own events",
+                   "parallelism": f"replicas x{world} (one independent batch per GPU)"},
+        "gpu_launches": int(launches), "clocks": clk.summary(),
+        "roofline": {"kernel": "count", "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                     "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                     "peak_source": "measured copy bandwidth" if pk["src"] == "measured" else "fallback",
+                     "traffic": None, "algorithmic_per_launch": float(nbytes)},
+        "kernels": {"count": {"us_per_step": round(ms * 1e3, 2), "launches_per_step": launches / args.steps,
+                              "GB/s": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm"], 4)}},
+        "e2e": {"value": round(job_throughput(wl.M, world, ms_e2e), 1), "unit": "tokens/s",
+                "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": int(ih.numel() * 4),
+                "d2h_bytes_per_step": int(ch.numel() * 4), "steps": n_e2e},
+    }
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -483,11 +565,18 @@ def oracle_sample(wl, target_s=12.0):
     """Times the CPU oracle (as it stands, single-threaded C) on a bounded sample of the
     workload: its first m tokens, m grown until one call takes ~target_s."""
     import oracle
-    li = mi.make_layer_inputs(wl)
+    count_only = wl.name == mi.COUNT_ONLY.name
+    if count_only:  # only the routing is needed
+        ids, w = mi.route(wl.M, wl.E, wl.topk, wl.seed, wl.zipf_s)
+        li = mi.LayerInputs(wl, np.zeros((wl.M, 0), np.uint16), ids, w, None)
+    else:
+        li = mi.make_layer_inputs(wl)
     m = 4
     while True:
         t0 = time.perf_counter()
-        if wl.N:
+        if count_only:
+            oracle.count(li.topk_ids[:m], wl.E, wl.El)
+        elif wl.N:
             oracle.forward_chunked(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], li.w13, li.w13_scale, li.w2,
                                    li.w2_scale, wl.E, expert_map=li.expert_map, chunk_size=wl.chunk)
         else:
@@ -513,7 +602,9 @@ def run_reference(args):
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        if wl.N:
+        if wl.name == mi.COUNT_ONLY.name:
+            oracle.count(li.topk_ids[:m], wl.E, wl.El)
+        elif wl.N:
             oracle.forward_chunked(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], li.w13, li.w13_scale, li.w2,
                                    li.w2_scale, wl.E, expert_map=li.expert_map, chunk_size=wl.chunk)
         else:
@@ -547,7 +638,10 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    line = run_ours(args, rank, world, local_rank)
+    if args.workload == mi.COUNT_ONLY.name:
+        line = run_count_only(args, world, local_rank)
+    else:
+        line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(mi.WORKLOADS[args.workload])

@@ -53,10 +53,11 @@ class Workload:
         return self.M if self.chunk_size is None else self.chunk_size
 
 
-# The five workloads: a tiny layer, a permute/unpermute-only pass, and a
+# The workloads: a tiny layer, a permute/unpermute-only pass, a
 # Qwen3-30B-A3B-shaped layer (hidden 2048, moe intermediate 768, 128 experts, top-8)
 # at decode size, at prefill size with skewed routing, and chunked with half the
-# experts local.
+# experts local, and a count-only pass over 2^20 tokens (33.5 MB of top-8 ids, large
+# enough for the count kernel's bandwidth to mean something).
 TINY = Workload("tiny_m64_k256_n256_e8_top2", M=64, K=256, N=256, E=8, topk=2, seed=0)
 PERMUTE_ONLY = Workload("permute_only_m4096_k2048_e128_top8", M=4096, K=2048, N=0,
                         E=128, topk=8, seed=2)
@@ -67,8 +68,10 @@ QWEN3_PREFILL = Workload("qwen3_30b_a3b_prefill_m8192_zipf1.2", M=8192, K=2048, 
 QWEN3_CHUNKED = Workload("qwen3_30b_a3b_chunked_m16385_c128_local64_zipf1.2", M=16385,
                          K=2048, N=768, E=128, topk=8, seed=5, zipf_s=1.2,
                          local_experts=64, chunk_size=128)
+COUNT_ONLY = Workload("count_only_m1048576_e128_top8", M=1 << 20, K=128, N=0, E=128, topk=8,
+                      seed=6)
 WORKLOADS = {w.name: w for w in (TINY, PERMUTE_ONLY, QWEN3_DECODE, QWEN3_PREFILL,
-                                 QWEN3_CHUNKED)}
+                                 QWEN3_CHUNKED, COUNT_ONLY)}
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:

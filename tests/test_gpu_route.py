@@ -43,7 +43,8 @@ def _local(E, local):
 
 
 @pytest.mark.parametrize("M,topk,E,local", SWEEP + [(5000, 8, 128, None), (70000, 8, 128, "half"),
-                                                   (300, 8, 128, "none_local"), (0, 8, 128, None)])
+                                                   (300, 8, 128, "none_local"), (0, 8, 128, None),
+                                                   (1 << 20, 8, 128, None)])  # the count-only benchmark's size
 def test_count_bit_exact(M, topk, E, local):
     ids, _, m, El = routing(M, topk, E, _local(E, local), seed=M + topk)
     ref, bad = oracle.count(ids, E, El, m)
