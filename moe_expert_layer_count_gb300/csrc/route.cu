@@ -228,9 +228,14 @@ __global__ void __launch_bounds__(kScatterThreads)
         } else {
             load_round(ids, r0, wend, expert_map, E, El, lane, l, bad);
         }
+        // per-warp counts: equal experts of a round are aggregated first (this pass sees
+        // few slots per warp, where a hot expert would serialise per-lane atomics)
 #pragma unroll
-        for (int j = 0; j < kRound; ++j)
-            if (l[j] >= 0) atomicAdd(&mine[l[j]], 1);
+        for (int j = 0; j < kRound; ++j) {
+            const unsigned m = __match_any_sync(0xffffffffu, l[j]);
+            if (l[j] >= 0 && lane == __ffs(m) - 1) mine[l[j]] += __popc(m);
+            __syncwarp();
+        }
     }
     if (derive && G == 1 && err_count) {
 #pragma unroll
