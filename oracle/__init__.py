@@ -76,6 +76,14 @@ def _c(a: np.ndarray, dtype) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=dtype)
 
 
+def _ids(topk_ids) -> np.ndarray:
+    """Top-k ids as int64 (the C side takes 64-bit ids; int32 ids widen exactly)."""
+    a = np.asarray(topk_ids)
+    if a.dtype.kind not in "iu":
+        raise TypeError(f"topk_ids: expected an integer array, got {a.dtype}")
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
 def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
@@ -105,7 +113,7 @@ def quant_rows(x: np.ndarray):
 # ----------------------------------------------------------------------- the steps
 def count(topk_ids, E, El, expert_map=None):
     """Step a1: tokens per local expert. Returns (counts int32 [El], n_bad_ids)."""
-    ids = _c(topk_ids, np.int32)
+    ids = _ids(topk_ids)
     M, topk = ids.shape
     m = None if expert_map is None else _c(expert_map, np.int32)
     counts = np.zeros(El, np.int32)
@@ -131,7 +139,7 @@ def scatter(x_bits, topk_ids, topk_weights, E, El, expert_map=None,
     """Step a2. Returns dict(a, a_scale, offsets, src2dst, bad); a is uint8 [Rp, K]
     (FP8 codes) when quant else uint16 bf16 bits [Rp, K]; padding rows are zero."""
     x = _c(x_bits, np.uint16)
-    ids = _c(topk_ids, np.int32)
+    ids = _ids(topk_ids)
     w = _c(topk_weights, np.float32)
     M, K = x.shape
     topk = ids.shape[1]
@@ -194,7 +202,7 @@ def forward_chunked(x_bits, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale
                     expert_map=None, chunk_size=None, apply_router_weight_on_input=False):
     """Step a7: the whole layer under the chunking loop, bf16 bits [M, K]."""
     x = _c(x_bits, np.uint16)
-    ids = _c(topk_ids, np.int32)
+    ids = _ids(topk_ids)
     w = _c(topk_weights, np.float32)
     w13 = _c(w13, np.uint8)
     s13 = _c(w13_scale, np.float32)
@@ -220,7 +228,7 @@ def forward_tokens(tokens, x_bits, topk_ids, topk_weights, w13, w13_scale, w2, w
     """The layer output of selected tokens, evaluated per token with no permutation.
     Returns bf16 bits [len(tokens), K]."""
     x = _c(x_bits, np.uint16)
-    ids = _c(topk_ids, np.int32)
+    ids = _ids(topk_ids)
     w = _c(topk_weights, np.float32)
     w13 = _c(w13, np.uint8)
     s13 = _c(w13_scale, np.float32)

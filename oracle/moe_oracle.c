@@ -117,8 +117,10 @@ void oracle_quant_row(const float* x, int K, uint8_t* q, float* scales) {
  * slice_expert_num_tokens(c_topk_ids, local_num_experts, expert_map)). expert_map maps
  * a global id to a local id or -1 (expert not on this GPU); with no map, local = global.
  * A slot is kept when its local id is in [0, El). Id -1 marks an empty slot and is
- * dropped silently; any other id outside [0, E) is dropped and counted as bad. */
-static int local_of(int32_t id, const int32_t* map, int E, int El, int64_t* bad) {
+ * dropped silently; any other id outside [0, E) is dropped and counted as bad. Ids are
+ * taken as 64-bit integers (int32 ids widen exactly), so an int64 id beyond the int32
+ * range is out of [0, E) like any other, never an alias of a small id. */
+static int local_of(int64_t id, const int32_t* map, int E, int El, int64_t* bad) {
     if (id == -1) return -1;
     if (id < 0 || id >= E) {
         ++*bad;
@@ -130,7 +132,7 @@ static int local_of(int32_t id, const int32_t* map, int E, int El, int64_t* bad)
 
 /* Step a1, count_expert_num_tokens (P3 Purpose, Bug 2): the number of (token, k) slots
  * routed to each local expert. Returns the number of bad ids. */
-int64_t oracle_count(const int32_t* topk_ids, int64_t M, int topk, const int32_t* expert_map, int E,
+int64_t oracle_count(const int64_t* topk_ids, int64_t M, int topk, const int32_t* expert_map, int E,
                      int El, int32_t* counts) {
     int64_t bad = 0;
     for (int l = 0; l < El; ++l) counts[l] = 0;
@@ -163,7 +165,7 @@ int64_t oracle_rp_cap(int64_t Mc, int topk, int El) {
  * on the input (P2 Changes, apply_router_weight_on_input). quant = 1: 1x128 FP8
  * codes + fp32 scales ([rows, K/128] row-major); quant = 0: a bf16 copy.
  * Padding rows are not written. Returns the number of bad ids. */
-int64_t oracle_scatter(const uint16_t* x, int64_t M, int K, const int32_t* topk_ids,
+int64_t oracle_scatter(const uint16_t* x, int64_t M, int K, const int64_t* topk_ids,
                        const float* topk_weights, int topk, const int32_t* expert_map, int E, int El,
                        int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
                        int32_t* offsets, int32_t* src2dst) {
@@ -299,7 +301,7 @@ static void expert_row(const uint8_t* a, const float* sa, int l, const uint8_t* 
  * of chunk_size; for each chunk the expert counts, offsets and workspace are derived
  * from that chunk's own topk_ids and the chunk runs a1..a6 on its own rows. out is
  * bf16 [M, K]. Returns the number of bad ids, or -1 on bad arguments. */
-int64_t oracle_forward_chunked(const uint16_t* x, const int32_t* topk_ids, const float* topk_weights,
+int64_t oracle_forward_chunked(const uint16_t* x, const int64_t* topk_ids, const float* topk_weights,
                                const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
                                const float* w2_scale, const int32_t* expert_map, int E, int El, int64_t M,
                                int K, int N, int topk, int64_t chunk_size, int apply_router_weight_on_input,
@@ -347,7 +349,7 @@ int64_t oracle_forward_chunked(const uint16_t* x, const int32_t* topk_ids, const
 /* The same layer output for one token t, evaluated directly from the definition with no
  * permutation at all: for each kept slot k, quantise the (weighted) input row, run the
  * expert, and accumulate w' * y in ascending k. out_row is bf16 [K]. */
-void oracle_forward_token(int64_t t, const uint16_t* x, const int32_t* topk_ids, const float* topk_weights,
+void oracle_forward_token(int64_t t, const uint16_t* x, const int64_t* topk_ids, const float* topk_weights,
                           const uint8_t* w13, const float* w13_scale, const uint8_t* w2, const float* w2_scale,
                           const int32_t* expert_map, int E, int El, int K, int N, int topk,
                           int apply_router_weight_on_input, uint16_t* out_row) {

@@ -178,6 +178,24 @@ def test_count_bad_ids_are_dropped_and_counted():
     assert list(counts) == [1, 2, 0, 0] and bad == 2
 
 
+def test_int64_ids_are_not_truncated():
+    """64-bit top-k ids follow the same rule: kept when in [0, E), -1 silent, anything
+    else dropped and counted. An id that would alias a small expert if cut to 32 bits
+    (2**32 + 1 -> 1) must be dropped, not counted for that expert."""
+    ids = np.array([[2**32 + 1, 1], [-1, 2**33], [-(2**32) + 2, 3], [2**62, 0]], np.int64)
+    counts, bad = oracle.count(ids, 4, 4)
+    assert list(counts) == [1, 1, 0, 1] and bad == 4
+    x = mi.bf16_bits(np.ones((4, 128), np.float32))
+    r = oracle.scatter(x, ids, np.full((4, 2), 0.5, np.float32), 4, 4, quant=False)
+    # kept slots (flat 1, 5, 7) in stable order within their experts; the rest dropped
+    assert list(r["src2dst"].reshape(-1)) == [-1, 128, -1, -1, -1, 256, -1, 0]
+    assert r["bad"] == 4
+    # ids that fit in 32 bits give the same answer from int32 and int64 arrays
+    small = np.array([[0, 3], [2, -1], [9, 1]], np.int64)
+    for got, want in zip(oracle.count(small, 4, 4), oracle.count(small.astype(np.int32), 4, 4)):
+        assert np.array_equal(got, want)
+
+
 def test_offsets_closed_form_and_rp_cap_bound():
     rng = np.random.default_rng(1)
     for _ in range(50):
