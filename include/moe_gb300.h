@@ -32,6 +32,10 @@
  *    kept when 0 <= l < local_num_experts. An id of -1 is an empty slot and is dropped
  *    silently; any other id outside [0, E) is dropped and counted in *err_count (when
  *    err_count is not NULL). Dropped slots take no row and add nothing to the output.
+ *  - topk_ids are int32. Every entry point that reads them has a twin with the suffix
+ *    _i64 that takes int64 ids (the dtype torch.topk returns) and is otherwise the same
+ *    call with the same results; an int64 id is range-checked at 64 bits, so an id such
+ *    as 2^32 + 1 is a bad id, never expert 1. Outputs (src2dst, counts) stay int32.
  *  - Permuted ("expert-contiguous") row space: expert l owns rows
  *    [expert_offsets[l], expert_offsets[l+1]), each offset a multiple of 128, and the
  *    first expert_num_tokens[l] rows of its block hold its slots in ascending
@@ -116,6 +120,10 @@ MOE_API size_t moe_workspace_size(int64_t chunk_M, int K, int N, int topk, int l
 MOE_API int moe_count_expert_tokens(const int32_t* topk_ids, int64_t M, int topk, const int32_t* expert_map,
                                     int E, int local_num_experts, int32_t* expert_num_tokens,
                                     int32_t* err_count, moe_stream_t stream);
+/* The same with topk_ids int64 [M, topk]. */
+MOE_API int moe_count_expert_tokens_i64(const int64_t* topk_ids, int64_t M, int topk, const int32_t* expert_map,
+                                        int E, int local_num_experts, int32_t* expert_num_tokens,
+                                        int32_t* err_count, moe_stream_t stream);
 
 /* ep_scatter / deepgemm_moe_permute ([P1] Purpose item 2), with the per-token FP8
  * activation quantisation ([P1] Optimizations: e4m3, 128 blocks) done in the same pass.
@@ -145,6 +153,13 @@ MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32
                         int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
                         int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, void* workspace,
                         size_t workspace_bytes, moe_stream_t stream);
+/* The same with topk_ids int64 [M, topk]. */
+MOE_API int moe_scatter_i64(const void* hidden_states, int64_t M, int K, const int64_t* topk_ids,
+                            const float* topk_weights, int topk, const int32_t* expert_map, int E,
+                            int local_num_experts, int32_t* expert_num_tokens, int count_here, int32_t* err_count,
+                            int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
+                            int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, void* workspace,
+                            size_t workspace_bytes, moe_stream_t stream);
 
 /* moe_scatter without a workspace argument, for callers that cannot allocate device
  * memory: for example an inference engine that plans every device buffer once at
@@ -170,6 +185,12 @@ MOE_API int moe_scatter_noalloc(const void* hidden_states, int64_t M, int K, con
                                 int local_num_experts, const int32_t* expert_num_tokens,
                                 int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
                                 int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, moe_stream_t stream);
+/* The same with topk_ids int64 [M, topk]. */
+MOE_API int moe_scatter_noalloc_i64(const void* hidden_states, int64_t M, int K, const int64_t* topk_ids,
+                                    const float* topk_weights, int topk, const int32_t* expert_map, int E,
+                                    int local_num_experts, const int32_t* expert_num_tokens,
+                                    int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
+                                    int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, moe_stream_t stream);
 
 /* The DeepGEMM-style grouped ("m-grouped contiguous") GEMM with 128x128 block-scaled
  * FP8 weights ([P1] Optimizations, --block-shape 128 128), on tcgen05 tensor cores:
@@ -242,11 +263,18 @@ MOE_API int moe_forward_chunked(const void* hidden_states, const int32_t* topk_i
                                 int64_t M, int K, int N, int topk, int64_t chunk_size,
                                 int apply_router_weight_on_input, void* out, void* workspace,
                                 size_t workspace_bytes, int32_t* err_count, moe_stream_t stream);
+/* The same with topk_ids int64 [M, topk]. */
+MOE_API int moe_forward_chunked_i64(const void* hidden_states, const int64_t* topk_ids, const float* topk_weights,
+                                    const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                    const float* w2_scale, const int32_t* expert_map, int E, int local_num_experts,
+                                    int64_t M, int K, int N, int topk, int64_t chunk_size,
+                                    int apply_router_weight_on_input, void* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* err_count, moe_stream_t stream);
 
-/* Workspace bytes moe_forward_host needs for batches of up to M tokens: the layer's own
- * workspace (moe_workspace_size for min(chunk_size, M)) followed by two staging slots,
- * each a device copy of a batch's hidden_states, topk_ids, topk_weights and output.
- * Returns 0 on bad arguments. */
+/* Workspace bytes moe_forward_host (or _i64) needs for batches of up to M tokens: the
+ * layer's own workspace (moe_workspace_size for min(chunk_size, M)) followed by two
+ * staging slots, each a device copy of a batch's hidden_states, topk_ids (room for int64
+ * ids), topk_weights and output. Returns 0 on bad arguments. */
 MOE_API size_t moe_host_workspace_size(int64_t M, int K, int N, int topk, int local_num_experts,
                                        int64_t chunk_size);
 
@@ -273,6 +301,13 @@ MOE_API int moe_forward_host(const void* hidden_states_host, const int32_t* topk
                              int local_num_experts, int64_t M, int K, int N, int topk, int64_t chunk_size,
                              int apply_router_weight_on_input, void* out_host, void* workspace,
                              size_t workspace_bytes, int32_t* err_count, moe_stream_t stream, moe_event_t done);
+/* The same with topk_ids_host int64 [M, topk] (host, page-locked). */
+MOE_API int moe_forward_host_i64(const void* hidden_states_host, const int64_t* topk_ids_host,
+                                 const float* topk_weights_host, const uint8_t* w13, const float* w13_scale,
+                                 const uint8_t* w2, const float* w2_scale, const int32_t* expert_map, int E,
+                                 int local_num_experts, int64_t M, int K, int N, int topk, int64_t chunk_size,
+                                 int apply_router_weight_on_input, void* out_host, void* workspace,
+                                 size_t workspace_bytes, int32_t* err_count, moe_stream_t stream, moe_event_t done);
 
 /* Makes `stream` wait until every output copy moe_forward_host has enqueued on the
  * current device so far has completed. */

@@ -58,18 +58,27 @@ SIGNATURES = {
     "moe_scatter_workspace_size": ([_i64, _int, _int], _sz),
     "moe_workspace_size": ([_i64, _int, _int, _int, _int], _sz),
     "moe_count_expert_tokens": ([_p, _i64, _int, _p, _int, _int, _p, _p, _p], _int),
+    "moe_count_expert_tokens_i64": ([_p, _i64, _int, _p, _int, _int, _p, _p, _p], _int),
     "moe_scatter": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _p, _int, _int, _p, _p, _p, _p,
                      _i64, _p, _sz, _p], _int),
+    "moe_scatter_i64": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _p, _int, _int, _p, _p, _p, _p,
+                         _i64, _p, _sz, _p], _int),
     "moe_scatter_noalloc": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _int, _p, _p, _p, _p, _i64,
                              _p], _int),
+    "moe_scatter_noalloc_i64": ([_p, _i64, _int, _p, _p, _int, _p, _int, _int, _p, _int, _int, _p, _p, _p, _p,
+                                 _i64, _p], _int),
     "moe_grouped_gemm_fp8": ([_p, _p, _p, _p, _p, _p, _int, _i64, _int, _int, _int, _p, _p, _p], _int),
     "moe_silu_mul_quant": ([_p, _p, _int, _i64, _int, _p, _p, _p], _int),
     "moe_gather_weight_reduce": ([_p, _p, _p, _i64, _int, _int, _int, _p, _p], _int),
     "moe_forward_chunked": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
                              _p, _p, _sz, _p, _p], _int),
+    "moe_forward_chunked_i64": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
+                                 _p, _p, _sz, _p, _p], _int),
     "moe_host_workspace_size": ([_i64, _int, _int, _int, _int, _i64], _sz),
     "moe_forward_host": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
                           _p, _p, _sz, _p, _p, _p], _int),
+    "moe_forward_host_i64": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
+                              _p, _p, _sz, _p, _p, _p], _int),
     "moe_host_wait": ([_p], _int),
 }
 
@@ -106,6 +115,15 @@ def _dt(t, dtype, name):
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
 
 
+def _ids_entry(name: str, topk_ids) -> str:
+    """The C entry point for the ids' dtype: `name` for int32, `name`_i64 for int64."""
+    if topk_ids.dtype == torch.int32:
+        return name
+    if topk_ids.dtype == torch.int64:
+        return name + "_i64"
+    raise TypeError(f"topk_ids: expected torch.int32 or torch.int64, got {topk_ids.dtype}")
+
+
 def status_string(status: int) -> str:
     return lib().moe_status_string(status).decode()
 
@@ -134,13 +152,13 @@ def moe_workspace_size(chunk_M: int, K: int, N: int, topk: int, local_num_expert
 # ------------------------------------------------------------------- entry points
 def moe_count_expert_tokens(topk_ids, E, local_num_experts, expert_map=None, expert_num_tokens=None,
                             err_count=None, stream=None):
-    """Tokens per local expert: int32 [local_num_experts]."""
-    _dt(topk_ids, torch.int32, "topk_ids")
+    """Tokens per local expert: int32 [local_num_experts]. topk_ids is int32 or int64."""
+    fn = _ids_entry("moe_count_expert_tokens", topk_ids)
     _dt(expert_map, torch.int32, "expert_map")
     M, topk = topk_ids.shape
     if expert_num_tokens is None:
         expert_num_tokens = torch.empty(local_num_experts, dtype=torch.int32, device=topk_ids.device)
-    _check("moe_count_expert_tokens", lib().moe_count_expert_tokens(
+    _check(fn, getattr(lib(), fn)(
         _ptr(topk_ids), M, topk, _ptr(expert_map), E, local_num_experts, _ptr(expert_num_tokens),
         _ptr(err_count), _stream(stream)))
     return expert_num_tokens
@@ -152,9 +170,9 @@ def moe_scatter(hidden_states, topk_ids, topk_weights, E, local_num_experts, exp
                 workspace=None, count_here=False, err_count=None, stream=None):
     """Permute rows into expert-contiguous, 128-aligned blocks (+ FP8 1x128 quant).
     With count_here, expert_num_tokens is an output (the count step fused into the
-    scatter). Returns (a_out, a_scale, expert_offsets, src2dst)."""
+    scatter). topk_ids is int32 or int64. Returns (a_out, a_scale, expert_offsets, src2dst)."""
     _dt(hidden_states, torch.bfloat16, "hidden_states")
-    _dt(topk_ids, torch.int32, "topk_ids")
+    fn = _ids_entry("moe_scatter", topk_ids)
     _dt(topk_weights, torch.float32, "topk_weights")
     M, K = hidden_states.shape
     topk = topk_ids.shape[1]
@@ -171,7 +189,7 @@ def moe_scatter(hidden_states, topk_ids, topk_weights, E, local_num_experts, exp
         src2dst = torch.empty(M, topk, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = torch.empty(moe_scatter_workspace_size(M, topk, El), dtype=torch.uint8, device=dev)
-    _check("moe_scatter", lib().moe_scatter(
+    _check(fn, getattr(lib(), fn)(
         _ptr(hidden_states), M, K, _ptr(topk_ids), _ptr(topk_weights), topk, _ptr(expert_map), E, El,
         _ptr(expert_num_tokens), int(bool(count_here)), _ptr(err_count), int(bool(apply_router_weight_on_input)),
         quant, _ptr(a_out), _ptr(a_scale), _ptr(expert_offsets), _ptr(src2dst), cap, _ptr(workspace),
@@ -184,13 +202,14 @@ def moe_scatter_noalloc(hidden_states, topk_ids, topk_weights, E, local_num_expe
                         apply_router_weight_on_input=False, quant=MOE_QUANT_FP8_1X128, rp_cap=None, stream=None):
     """moe_scatter for callers that cannot allocate: every output buffer is the caller's,
     and the scratch is a fixed array inside the library (see the C header for its limit
-    and for the rule that calls must not overlap on the GPU). Returns the outputs."""
+    and for the rule that calls must not overlap on the GPU). topk_ids is int32 or int64.
+    Returns the outputs."""
     _dt(hidden_states, torch.bfloat16, "hidden_states")
-    _dt(topk_ids, torch.int32, "topk_ids")
+    fn = _ids_entry("moe_scatter_noalloc", topk_ids)
     M, K = hidden_states.shape
     topk = topk_ids.shape[1]
     cap = a_out.shape[0] if rp_cap is None else rp_cap
-    _check("moe_scatter_noalloc", lib().moe_scatter_noalloc(
+    _check(fn, getattr(lib(), fn)(
         _ptr(hidden_states), M, K, _ptr(topk_ids), _ptr(topk_weights), topk, _ptr(expert_map), E,
         local_num_experts, _ptr(expert_num_tokens), int(bool(apply_router_weight_on_input)), quant,
         _ptr(a_out), _ptr(a_scale), _ptr(expert_offsets), _ptr(src2dst), cap, _stream(stream)))
@@ -253,9 +272,9 @@ def moe_gather_weight_reduce(y, src2dst, topk_weights, apply_router_weight_on_in
 def moe_forward_chunked(hidden_states, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, E,
                         expert_map=None, chunk_size=None, apply_router_weight_on_input=False, out=None,
                         workspace=None, err_count=None, stream=None):
-    """The whole MoE layer under the chunking loop: bf16 [M, K]."""
+    """The whole MoE layer under the chunking loop: bf16 [M, K]. topk_ids is int32 or int64."""
     _dt(hidden_states, torch.bfloat16, "hidden_states")
-    _dt(topk_ids, torch.int32, "topk_ids")
+    fn = _ids_entry("moe_forward_chunked", topk_ids)
     _dt(topk_weights, torch.float32, "topk_weights")
     M, K = hidden_states.shape
     El, N2, _ = w13.shape
@@ -266,7 +285,7 @@ def moe_forward_chunked(hidden_states, topk_ids, topk_weights, w13, w13_scale, w
     if workspace is None:
         workspace = torch.empty(max(1, moe_workspace_size(max(1, min(chunk, M)), K, N2 // 2, topk, El)),
                                 dtype=torch.uint8, device=hidden_states.device)
-    _check("moe_forward_chunked", lib().moe_forward_chunked(
+    _check(fn, getattr(lib(), fn)(
         _ptr(hidden_states), _ptr(topk_ids), _ptr(topk_weights), _ptr(w13), _ptr(w13_scale), _ptr(w2),
         _ptr(w2_scale), _ptr(expert_map), E, El, M, K, N2 // 2, topk, max(1, chunk),
         int(bool(apply_router_weight_on_input)), _ptr(out), _ptr(workspace), workspace.numel(),
@@ -303,9 +322,9 @@ def moe_forward_host(hidden_states, topk_ids, topk_weights, w13, w13_scale, w2, 
     """The layer with the batch in pinned HOST memory (hidden_states, topk_ids,
     topk_weights and out are pinned CPU tensors); asynchronous: `out` holds the result
     once the torch.cuda.Event `done` has completed, or once the stream has passed a later
-    moe_host_wait()."""
+    moe_host_wait(). topk_ids is int32 or int64."""
     _dt(hidden_states, torch.bfloat16, "hidden_states")
-    _dt(topk_ids, torch.int32, "topk_ids")
+    fn = _ids_entry("moe_forward_host", topk_ids)
     _dt(topk_weights, torch.float32, "topk_weights")
     M, K = hidden_states.shape
     El, N2, _ = w13.shape
@@ -316,7 +335,7 @@ def moe_forward_host(hidden_states, topk_ids, topk_weights, w13, w13_scale, w2, 
     if workspace is None:
         workspace = torch.empty(max(1, moe_host_workspace_size(max(1, M), K, N2 // 2, topk, El, max(1, chunk))),
                                 dtype=torch.uint8, device=w13.device)
-    _check("moe_forward_host", lib().moe_forward_host(
+    _check(fn, getattr(lib(), fn)(
         _hptr(hidden_states), _hptr(topk_ids), _hptr(topk_weights), _ptr(w13), _ptr(w13_scale), _ptr(w2),
         _ptr(w2_scale), _ptr(expert_map), E, El, M, K, N2 // 2, topk, max(1, chunk),
         int(bool(apply_router_weight_on_input)), _hptr(out), _ptr(workspace), workspace.numel(),

@@ -117,9 +117,15 @@ MOE_API size_t moe_workspace_size(int64_t chunk_M, int K, int N, int topk, int l
     return carve(chunk_M, K, N, topk, local_num_experts).total;
 }
 
-MOE_API int moe_count_expert_tokens(const int32_t* topk_ids, int64_t M, int topk, const int32_t* expert_map, int E,
-                                    int local_num_experts, int32_t* expert_num_tokens, int32_t* err_count,
-                                    moe_stream_t stream) {
+}  // extern "C"
+
+// The entry points that read top-k ids, for either id type (the _i64 exports take int64).
+namespace moe {
+namespace {
+
+template <typename TId>
+int count_impl(const TId* topk_ids, int64_t M, int topk, const int32_t* expert_map, int E, int local_num_experts,
+               int32_t* expert_num_tokens, int32_t* err_count, moe_stream_t stream) {
     if (!routing_args_ok(M, topk, E, local_num_experts) || !expert_num_tokens || (M > 0 && !topk_ids))
         return MOE_ERR_INVALID_ARG;
     int sms = 0;
@@ -128,12 +134,12 @@ MOE_API int moe_count_expert_tokens(const int32_t* topk_ids, int64_t M, int topk
                         (cudaStream_t)stream);
 }
 
-MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32_t* topk_ids,
-                        const float* topk_weights, int topk, const int32_t* expert_map, int E, int local_num_experts,
-                        int32_t* expert_num_tokens, int count_here, int32_t* err_count,
-                        int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
-                        int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, void* workspace,
-                        size_t workspace_bytes, moe_stream_t stream) {
+template <typename TId>
+int scatter_impl(const void* hidden_states, int64_t M, int K, const TId* topk_ids, const float* topk_weights,
+                 int topk, const int32_t* expert_map, int E, int local_num_experts, int32_t* expert_num_tokens,
+                 int count_here, int32_t* err_count, int apply_router_weight_on_input, int quant, void* a_out,
+                 float* a_scale, int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, void* workspace,
+                 size_t workspace_bytes, moe_stream_t stream) {
     if (!routing_args_ok(M, topk, E, local_num_experts) || K <= 0 || K % kGroup || !expert_num_tokens ||
         !expert_offsets || (quant != MOE_QUANT_NONE && quant != MOE_QUANT_FP8_1X128))
         return MOE_ERR_INVALID_ARG;
@@ -153,6 +159,45 @@ MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32
                           count_here ? expert_num_tokens : nullptr, count_here ? err_count : nullptr,
                           apply_router_weight_on_input ? 1 : 0, quant, a_out, a_scale, expert_offsets, src2dst,
                           static_cast<int32_t*>(workspace), (cudaStream_t)stream);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+MOE_API int moe_count_expert_tokens(const int32_t* topk_ids, int64_t M, int topk, const int32_t* expert_map, int E,
+                                    int local_num_experts, int32_t* expert_num_tokens, int32_t* err_count,
+                                    moe_stream_t stream) {
+    return count_impl(topk_ids, M, topk, expert_map, E, local_num_experts, expert_num_tokens, err_count, stream);
+}
+
+MOE_API int moe_count_expert_tokens_i64(const int64_t* topk_ids, int64_t M, int topk, const int32_t* expert_map,
+                                        int E, int local_num_experts, int32_t* expert_num_tokens, int32_t* err_count,
+                                        moe_stream_t stream) {
+    return count_impl(topk_ids, M, topk, expert_map, E, local_num_experts, expert_num_tokens, err_count, stream);
+}
+
+MOE_API int moe_scatter(const void* hidden_states, int64_t M, int K, const int32_t* topk_ids,
+                        const float* topk_weights, int topk, const int32_t* expert_map, int E, int local_num_experts,
+                        int32_t* expert_num_tokens, int count_here, int32_t* err_count,
+                        int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
+                        int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, void* workspace,
+                        size_t workspace_bytes, moe_stream_t stream) {
+    return scatter_impl(hidden_states, M, K, topk_ids, topk_weights, topk, expert_map, E, local_num_experts,
+                        expert_num_tokens, count_here, err_count, apply_router_weight_on_input, quant, a_out, a_scale,
+                        expert_offsets, src2dst, rp_cap, workspace, workspace_bytes, stream);
+}
+
+MOE_API int moe_scatter_i64(const void* hidden_states, int64_t M, int K, const int64_t* topk_ids,
+                            const float* topk_weights, int topk, const int32_t* expert_map, int E,
+                            int local_num_experts, int32_t* expert_num_tokens, int count_here, int32_t* err_count,
+                            int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
+                            int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, void* workspace,
+                            size_t workspace_bytes, moe_stream_t stream) {
+    return scatter_impl(hidden_states, M, K, topk_ids, topk_weights, topk, expert_map, E, local_num_experts,
+                        expert_num_tokens, count_here, err_count, apply_router_weight_on_input, quant, a_out, a_scale,
+                        expert_offsets, src2dst, rp_cap, workspace, workspace_bytes, stream);
 }
 
 MOE_API int moe_grouped_gemm_fp8(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
@@ -200,6 +245,33 @@ MOE_API int moe_forward_chunked(const void* hidden_states, const int32_t* topk_i
                                 const int32_t* expert_map, int E, int local_num_experts, int64_t M, int K, int N,
                                 int topk, int64_t chunk_size, int apply_router_weight_on_input, void* out,
                                 void* workspace, size_t workspace_bytes, int32_t* err_count, moe_stream_t stream) {
+    return forward_chunked_impl(hidden_states, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, expert_map, E,
+                                local_num_experts, M, K, N, topk, chunk_size, apply_router_weight_on_input, out,
+                                workspace, workspace_bytes, err_count, stream);
+}
+
+MOE_API int moe_forward_chunked_i64(const void* hidden_states, const int64_t* topk_ids, const float* topk_weights,
+                                    const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                    const float* w2_scale, const int32_t* expert_map, int E, int local_num_experts,
+                                    int64_t M, int K, int N, int topk, int64_t chunk_size,
+                                    int apply_router_weight_on_input, void* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* err_count, moe_stream_t stream) {
+    return forward_chunked_impl(hidden_states, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, expert_map, E,
+                                local_num_experts, M, K, N, topk, chunk_size, apply_router_weight_on_input, out,
+                                workspace, workspace_bytes, err_count, stream);
+}
+
+}  // extern "C"
+
+namespace moe {
+
+// The chunking loop, for either top-k id type.
+template <typename TId>
+int forward_chunked_impl(const void* hidden_states, const TId* topk_ids, const float* topk_weights,
+                         const uint8_t* w13, const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                         const int32_t* expert_map, int E, int local_num_experts, int64_t M, int K, int N, int topk,
+                         int64_t chunk_size, int apply_router_weight_on_input, void* out, void* workspace,
+                         size_t workspace_bytes, int32_t* err_count, moe_stream_t stream) {
     if (!routing_args_ok(M, topk, E, local_num_experts) || K <= 0 || N <= 0 || K % kGroup || N % kGroup ||
         chunk_size < 1)
         return MOE_ERR_INVALID_ARG;
@@ -239,7 +311,7 @@ MOE_API int moe_forward_chunked(const void* hidden_states, const int32_t* topk_i
         uint16_t* Y = reinterpret_cast<uint16_t*>(ws + cv.y);
         uint8_t* H = ws + cv.h;
         float* sh = reinterpret_cast<float*>(ws + cv.h_scale);
-        const int32_t* ids = topk_ids + c0 * topk;
+        const TId* ids = topk_ids + c0 * topk;
         const float* tw = topk_weights + c0 * topk;
         // the chunk's expert counts come out of the scatter's own histogram pass
         int st = launch_scatter(x + c0 * K, Mc, K, ids, tw, topk, expert_map, E, El, nullptr, counts, err_count,
@@ -255,4 +327,11 @@ MOE_API int moe_forward_chunked(const void* hidden_states, const int32_t* topk_i
     return MOE_OK;
 }
 
-}  // extern "C"
+template int forward_chunked_impl<int32_t>(const void*, const int32_t*, const float*, const uint8_t*, const float*,
+                                           const uint8_t*, const float*, const int32_t*, int, int, int64_t, int, int,
+                                           int, int64_t, int, void*, void*, size_t, int32_t*, moe_stream_t);
+template int forward_chunked_impl<int64_t>(const void*, const int64_t*, const float*, const uint8_t*, const float*,
+                                           const uint8_t*, const float*, const int32_t*, int, int, int64_t, int, int,
+                                           int, int64_t, int, void*, void*, size_t, int32_t*, moe_stream_t);
+
+}  // namespace moe

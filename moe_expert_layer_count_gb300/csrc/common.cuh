@@ -61,14 +61,17 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Local expert of a top-k id; -1 when dropped. Bad ids (outside [-1, E)) bump *bad.
-__device__ __forceinline__ int local_expert(int id, const int32_t* __restrict__ expert_map, int E, int El, int& bad) {
-    if (id == -1) return -1;
-    if (id < 0 || id >= E) {
+// Local expert of a top-k id (int32 or int64); -1 when dropped. Bad ids (outside
+// [-1, E)) bump *bad; the range test is done at the id's own width, so a 64-bit id never
+// aliases a small expert.
+template <typename TId>
+__device__ __forceinline__ int local_expert(TId id, const int32_t* __restrict__ expert_map, int E, int El, int& bad) {
+    if (id == TId(-1)) return -1;
+    if (id < 0 || id >= TId(E)) {
         ++bad;
         return -1;
     }
-    int l = expert_map ? __ldg(expert_map + id) : id;
+    int l = expert_map ? __ldg(expert_map + id) : (int)id;
     return (l >= 0 && l < El) ? l : -1;
 }
 

@@ -39,7 +39,8 @@ HostPipe g_pipe[kMaxDevices];
 
 inline size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
-// Byte layout of one staging slot for a batch of M tokens.
+// Byte layout of one staging slot for a batch of M tokens. The ids region has room for
+// 8-byte ids, so one workspace size serves both id types.
 struct Slot {
     size_t x, ids, w, out, total;
 };
@@ -47,7 +48,7 @@ Slot slot_layout(int64_t M, int K, int topk) {
     Slot s{};
     size_t p = 0;
     s.x = p;   p += align256((size_t)M * K * 2);
-    s.ids = p; p += align256((size_t)M * topk * 4);
+    s.ids = p; p += align256((size_t)M * topk * 8);
     s.w = p;   p += align256((size_t)M * topk * 4);
     s.out = p; p += align256((size_t)M * K * 2);
     s.total = p;
@@ -75,22 +76,23 @@ int pipe_init(HostPipe& p) {
 
 using namespace moe;
 
-extern "C" {
-
-MOE_API size_t moe_host_workspace_size(int64_t M, int K, int N, int topk, int local_num_experts,
-                                       int64_t chunk_size) {
+extern "C" MOE_API size_t moe_host_workspace_size(int64_t M, int K, int N, int topk, int local_num_experts,
+                                                  int64_t chunk_size) {
     if (M < 1 || K <= 0 || N <= 0 || topk < 1 || local_num_experts < 1 || chunk_size < 1) return 0;
     const size_t layer = moe_workspace_size(chunk_size < M ? chunk_size : M, K, N, topk, local_num_experts);
     if (!layer) return 0;
     return align256(layer) + 2 * slot_layout(M, K, topk).total;
 }
 
-MOE_API int moe_forward_host(const void* hidden_states_host, const int32_t* topk_ids_host,
-                             const float* topk_weights_host, const uint8_t* w13, const float* w13_scale,
-                             const uint8_t* w2, const float* w2_scale, const int32_t* expert_map, int E,
-                             int local_num_experts, int64_t M, int K, int N, int topk, int64_t chunk_size,
-                             int apply_router_weight_on_input, void* out_host, void* workspace,
-                             size_t workspace_bytes, int32_t* err_count, moe_stream_t stream, moe_event_t done) {
+namespace moe {
+namespace {
+
+template <typename TId>
+int forward_host_impl(const void* hidden_states_host, const TId* topk_ids_host, const float* topk_weights_host,
+                      const uint8_t* w13, const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                      const int32_t* expert_map, int E, int local_num_experts, int64_t M, int K, int N, int topk,
+                      int64_t chunk_size, int apply_router_weight_on_input, void* out_host, void* workspace,
+                      size_t workspace_bytes, int32_t* err_count, moe_stream_t stream, moe_event_t done) {
     if (M < 0 || K <= 0 || N <= 0 || topk < 1 || topk > 32 || E < 1 || local_num_experts < 1 || chunk_size < 1)
         return MOE_ERR_INVALID_ARG;
     if (M == 0) return MOE_OK;
@@ -112,7 +114,7 @@ MOE_API int moe_forward_host(const void* hidden_states_host, const int32_t* topk
     const int s = (int)(p.calls & 1u);
     uint8_t* base = static_cast<uint8_t*>(workspace) + layer_bytes + (size_t)s * L.total;
     void* x = base + L.x;
-    int32_t* ids = reinterpret_cast<int32_t*>(base + L.ids);
+    TId* ids = reinterpret_cast<TId*>(base + L.ids);
     float* w = reinterpret_cast<float*>(base + L.w);
     void* out = base + L.out;
     cudaStream_t cs = (cudaStream_t)stream;
@@ -120,15 +122,15 @@ MOE_API int moe_forward_host(const void* hidden_states_host, const int32_t* topk
     // inputs into the slot, once its previous use has been copied out
     if (cudaStreamWaitEvent(p.h2d, p.out_done[s], 0) != cudaSuccess ||
         cudaMemcpyAsync(x, hidden_states_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, p.h2d) != cudaSuccess ||
-        cudaMemcpyAsync(ids, topk_ids_host, (size_t)M * topk * 4, cudaMemcpyHostToDevice, p.h2d) != cudaSuccess ||
+        cudaMemcpyAsync(ids, topk_ids_host, (size_t)M * topk * sizeof(TId), cudaMemcpyHostToDevice, p.h2d) != cudaSuccess ||
         cudaMemcpyAsync(w, topk_weights_host, (size_t)M * topk * 4, cudaMemcpyHostToDevice, p.h2d) != cudaSuccess ||
         cudaEventRecord(p.in_done[s], p.h2d) != cudaSuccess)
         return MOE_ERR_CUDA;
     // the layer on the caller's stream, after the inputs have landed
     if (cudaStreamWaitEvent(cs, p.in_done[s], 0) != cudaSuccess) return MOE_ERR_CUDA;
-    int st = moe_forward_chunked(x, ids, w, w13, w13_scale, w2, w2_scale, expert_map, E, local_num_experts, M, K, N,
-                                 topk, chunk_size, apply_router_weight_on_input, out, workspace, layer_bytes,
-                                 err_count, stream);
+    int st = forward_chunked_impl(x, ids, w, w13, w13_scale, w2, w2_scale, expert_map, E, local_num_experts, M, K,
+                                  N, topk, chunk_size, apply_router_weight_on_input, out, workspace, layer_bytes,
+                                  err_count, cs);
     if (st) return st;
     // the output back to the host, after the layer
     if (cudaEventRecord(p.compute_done[s], cs) != cudaSuccess ||
@@ -140,6 +142,35 @@ MOE_API int moe_forward_host(const void* hidden_states_host, const int32_t* topk
     p.last = s;
     ++p.calls;
     return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+MOE_API int moe_forward_host(const void* hidden_states_host, const int32_t* topk_ids_host,
+                             const float* topk_weights_host, const uint8_t* w13, const float* w13_scale,
+                             const uint8_t* w2, const float* w2_scale, const int32_t* expert_map, int E,
+                             int local_num_experts, int64_t M, int K, int N, int topk, int64_t chunk_size,
+                             int apply_router_weight_on_input, void* out_host, void* workspace,
+                             size_t workspace_bytes, int32_t* err_count, moe_stream_t stream, moe_event_t done) {
+    return forward_host_impl(hidden_states_host, topk_ids_host, topk_weights_host, w13, w13_scale, w2, w2_scale,
+                             expert_map, E, local_num_experts, M, K, N, topk, chunk_size,
+                             apply_router_weight_on_input, out_host, workspace, workspace_bytes, err_count, stream,
+                             done);
+}
+
+MOE_API int moe_forward_host_i64(const void* hidden_states_host, const int64_t* topk_ids_host,
+                                 const float* topk_weights_host, const uint8_t* w13, const float* w13_scale,
+                                 const uint8_t* w2, const float* w2_scale, const int32_t* expert_map, int E,
+                                 int local_num_experts, int64_t M, int K, int N, int topk, int64_t chunk_size,
+                                 int apply_router_weight_on_input, void* out_host, void* workspace,
+                                 size_t workspace_bytes, int32_t* err_count, moe_stream_t stream, moe_event_t done) {
+    return forward_host_impl(hidden_states_host, topk_ids_host, topk_weights_host, w13, w13_scale, w2, w2_scale,
+                             expert_map, E, local_num_experts, M, K, N, topk, chunk_size,
+                             apply_router_weight_on_input, out_host, workspace, workspace_bytes, err_count, stream,
+                             done);
 }
 
 MOE_API int moe_host_wait(moe_stream_t stream) {

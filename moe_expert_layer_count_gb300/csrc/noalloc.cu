@@ -40,17 +40,12 @@ int scratch_address(int32_t** out) {
     return MOE_OK;
 }
 
-}  // namespace
-}  // namespace moe
-
-using namespace moe;
-
-extern "C" MOE_API int moe_scatter_noalloc(const void* hidden_states, int64_t M, int K, const int32_t* topk_ids,
-                                           const float* topk_weights, int topk, const int32_t* expert_map, int E,
-                                           int local_num_experts, const int32_t* expert_num_tokens,
-                                           int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
-                                           int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap,
-                                           moe_stream_t stream) {
+template <typename TId>
+int scatter_noalloc_impl(const void* hidden_states, int64_t M, int K, const TId* topk_ids, const float* topk_weights,
+                         int topk, const int32_t* expert_map, int E, int local_num_experts,
+                         const int32_t* expert_num_tokens, int apply_router_weight_on_input, int quant, void* a_out,
+                         float* a_scale, int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap,
+                         moe_stream_t stream) {
     if (M < 0 || topk < 1 || topk > 32 || E < 1 || local_num_experts < 1 || local_num_experts > kMaxLocalExperts ||
         K <= 0 || K % kGroup || !expert_num_tokens || !expert_offsets ||
         (quant != MOE_QUANT_NONE && quant != MOE_QUANT_FP8_1X128))
@@ -81,3 +76,32 @@ extern "C" MOE_API int moe_scatter_noalloc(const void* hidden_states, int64_t M,
                           apply_router_weight_on_input ? 1 : 0, quant, a_out, a_scale, expert_offsets, src2dst, scratch,
                           (cudaStream_t)stream);
 }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+MOE_API int moe_scatter_noalloc(const void* hidden_states, int64_t M, int K, const int32_t* topk_ids,
+                                const float* topk_weights, int topk, const int32_t* expert_map, int E,
+                                int local_num_experts, const int32_t* expert_num_tokens,
+                                int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
+                                int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, moe_stream_t stream) {
+    return scatter_noalloc_impl(hidden_states, M, K, topk_ids, topk_weights, topk, expert_map, E, local_num_experts,
+                                expert_num_tokens, apply_router_weight_on_input, quant, a_out, a_scale,
+                                expert_offsets, src2dst, rp_cap, stream);
+}
+
+MOE_API int moe_scatter_noalloc_i64(const void* hidden_states, int64_t M, int K, const int64_t* topk_ids,
+                                    const float* topk_weights, int topk, const int32_t* expert_map, int E,
+                                    int local_num_experts, const int32_t* expert_num_tokens,
+                                    int apply_router_weight_on_input, int quant, void* a_out, float* a_scale,
+                                    int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, moe_stream_t stream) {
+    return scatter_noalloc_impl(hidden_states, M, K, topk_ids, topk_weights, topk, expert_map, E, local_num_experts,
+                                expert_num_tokens, apply_router_weight_on_input, quant, a_out, a_scale,
+                                expert_offsets, src2dst, rp_cap, stream);
+}
+
+}  // extern "C"

@@ -14,18 +14,20 @@ namespace moe {
 
 // ------------------------------------------------------------------------ count
 // One CTA builds a shared-memory histogram of its share of the top-k slots (16-byte
-// id loads, four per thread issued back to back), one shared atomic per slot into one
+// id loads: four int32 or two int64 ids each, four loads per thread issued back to
+// back), one shared atomic per slot into one
 // of kCountCopies sub-histograms (warp w uses copy w % kCountCopies, so that only lanes
 // of one warp can collide on a popular expert), then sums the copies and stores the
 // result (single CTA) or adds it to the zeroed global counts (one global atomic per CTA
 // and expert). Aggregating equal experts with __match_any_sync first measured 2-4x
 // slower: its cost per call exceeds the atomics it saves.
 constexpr int kCountCopies = 8;
-template <int kThreads>
+template <int kThreads, typename TId>
 __global__ void __launch_bounds__(kThreads)
-    count_kernel(const int32_t* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E, int El,
+    count_kernel(const TId* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E, int El,
                  int32_t* __restrict__ counts, int32_t* __restrict__ err_count, int direct) {
-    constexpr int kVec = 4;  // int4 loads in flight per thread
+    constexpr int kVec = 4;                      // 16-byte loads in flight per thread
+    constexpr int kPer = 16 / (int)sizeof(TId);  // ids per 16-byte load
     extern __shared__ int32_t hist[];  // kCountCopies sub-histograms of El entries
     for (int l = threadIdx.x; l < kCountCopies * El; l += kThreads) hist[l] = 0;
     pdl_wait();
@@ -37,26 +39,33 @@ __global__ void __launch_bounds__(kThreads)
     auto add = [&](int l) {
         if (l >= 0) atomicAdd(&mine[l], 1);
     };
+    // the ids of one 16-byte load (little-endian: an int64 id's low word comes first)
+    auto add16 = [&](const uint4& v) {
+        if constexpr (kPer == 4) {
+            add(local_expert((int32_t)v.x, expert_map, E, El, bad));
+            add(local_expert((int32_t)v.y, expert_map, E, El, bad));
+            add(local_expert((int32_t)v.z, expert_map, E, El, bad));
+            add(local_expert((int32_t)v.w, expert_map, E, El, bad));
+        } else {
+            add(local_expert((int64_t)(((uint64_t)v.y << 32) | v.x), expert_map, E, El, bad));
+            add(local_expert((int64_t)(((uint64_t)v.w << 32) | v.z), expert_map, E, El, bad));
+        }
+    };
     const bool vec = (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
-    const int64_t n4 = vec ? n / 4 : 0;
-    const int4* ids4 = reinterpret_cast<const int4*>(ids);
+    const int64_t n4 = vec ? n / kPer : 0;
+    const uint4* ids4 = reinterpret_cast<const uint4*>(ids);
     const int64_t step = (int64_t)gridDim.x * kThreads * kVec;
     for (int64_t b0 = (int64_t)blockIdx.x * kThreads * kVec + (threadIdx.x & ~31) * kVec; b0 < n4; b0 += step) {
-        int4 v[kVec];
+        uint4 v[kVec];
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
             const int64_t i = b0 + j * 32 + lane;
-            v[j] = i < n4 ? __ldg(ids4 + i) : make_int4(-1, -1, -1, -1);
+            v[j] = i < n4 ? __ldg(ids4 + i) : make_uint4(~0u, ~0u, ~0u, ~0u);  // all ids -1
         }
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            add(local_expert(v[j].x, expert_map, E, El, bad));
-            add(local_expert(v[j].y, expert_map, E, El, bad));
-            add(local_expert(v[j].z, expert_map, E, El, bad));
-            add(local_expert(v[j].w, expert_map, E, El, bad));
-        }
+        for (int j = 0; j < kVec; ++j) add16(v[j]);
     }
-    for (int64_t i0 = 4 * n4 + (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); i0 < n;
+    for (int64_t i0 = kPer * n4 + (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); i0 < n;
          i0 += (int64_t)gridDim.x * kThreads) {
         const int64_t i = i0 + lane;
         add(i < n ? local_expert(__ldg(ids + i), expert_map, E, El, bad) : -1);
@@ -78,22 +87,28 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-int launch_count(const int32_t* ids, int64_t n, const int32_t* expert_map, int E, int El, int32_t* counts,
+template <typename TId>
+int launch_count(const TId* ids, int64_t n, const int32_t* expert_map, int E, int El, int32_t* counts,
                  int32_t* err_count, int num_sms, cudaStream_t stream) {
     const size_t smem = (size_t)kCountCopies * El * sizeof(int32_t);
-    if (n <= 16384) {  // one CTA, one batch of loads per thread: no memset needed
-        launch_k(count_kernel<1024>, 1, 1024, smem, stream, ids, n, expert_map, E, El, counts, err_count, 1);
+    if (n <= 16384) {  // one CTA, one (int32) or two (int64) batches of loads per thread: no memset needed
+        launch_k(count_kernel<1024, TId>, 1, 1024, smem, stream, ids, n, expert_map, E, El, counts, err_count, 1);
         note_launches(1);
         return launch_status();
     }
-    // 256-thread CTAs, 4096 slots each (one batch of 16 ids per thread), adding into zeros
+    // 256-thread CTAs, 4096 slots each (16 ids per thread: one batch of int32 ids, two of
+    // int64), adding into zeros
     if (cudaMemsetAsync(counts, 0, (size_t)El * sizeof(int32_t), stream) != cudaSuccess) return MOE_ERR_CUDA;
     const int64_t want = (n + 4095) / 4096;
     const int grid = (int)(want < 4 * num_sms ? want : 4 * num_sms);
-    launch_k(count_kernel<256>, grid, 256, smem, stream, ids, n, expert_map, E, El, counts, err_count, 0);
+    launch_k(count_kernel<256, TId>, grid, 256, smem, stream, ids, n, expert_map, E, El, counts, err_count, 0);
     note_launches(1);
     return launch_status();
 }
+template int launch_count<int32_t>(const int32_t*, int64_t, const int32_t*, int, int, int32_t*, int32_t*, int,
+                                   cudaStream_t);
+template int launch_count<int64_t>(const int64_t*, int64_t, const int32_t*, int, int, int32_t*, int32_t*, int,
+                                   cudaStream_t);
 
 // ---------------------------------------------------------------------- scatter
 // The stable permutation is a counting sort over the flat slot index i = t*topk + k:
@@ -116,21 +131,23 @@ int scatter_slots_per_cta(int64_t n) {
 }
 
 // Local experts of one round of a warp's segment: slot base + 32 j + lane, j < kRound.
-__device__ __forceinline__ void load_round(const int32_t* __restrict__ ids, int64_t base, int64_t end,
+template <typename TId>
+__device__ __forceinline__ void load_round(const TId* __restrict__ ids, int64_t base, int64_t end,
                                            const int32_t* __restrict__ expert_map, int E, int El, int lane,
                                            int (&l)[kRound], int& bad) {
-    int id[kRound];
+    TId id[kRound];
 #pragma unroll
     for (int j = 0; j < kRound; ++j) {
         const int64_t i = base + j * 32 + lane;
-        id[j] = i < end ? __ldg(ids + i) : -1;
+        id[j] = i < end ? __ldg(ids + i) : TId(-1);
     }
 #pragma unroll
     for (int j = 0; j < kRound; ++j) l[j] = local_expert(id[j], expert_map, E, El, bad);
 }
 
+template <typename TId>
 __global__ void __launch_bounds__(kScatterThreads)
-    scatter_hist_kernel(const int32_t* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E,
+    scatter_hist_kernel(const TId* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E,
                         int El, int per_cta, int32_t* __restrict__ hist, int32_t* __restrict__ err_count) {
     extern __shared__ int32_t sh[];  // kCountCopies sub-histograms of El entries
     for (int l = threadIdx.x; l < kCountCopies * El; l += kScatterThreads) sh[l] = 0;
@@ -167,8 +184,9 @@ __global__ void __launch_bounds__(kScatterThreads)
 // counts_in: the experts' slot counts (moe_scatter's input). When it is NULL the counts
 // are derived here -- from all CTAs' histograms, or from this single CTA's own pass --
 // and written to counts_out (the chunk loop's count step, fused into the scatter).
+template <typename TId>
 __global__ void __launch_bounds__(kScatterThreads)
-    scatter_rank_kernel(const int32_t* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E,
+    scatter_rank_kernel(const TId* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E,
                         int El, int per_cta, const int32_t* __restrict__ counts_in, const int32_t* __restrict__ hist,
                         int32_t* __restrict__ expert_offsets, int32_t* __restrict__ src2dst,
                         int32_t* __restrict__ counts_out, int32_t* __restrict__ err_count) {
@@ -394,7 +412,8 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-int launch_scatter(const uint16_t* x, int64_t M, int K, const int32_t* ids, const float* topk_weights, int topk,
+template <typename TId>
+int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const float* topk_weights, int topk,
                    const int32_t* expert_map, int E, int El, const int32_t* counts_in, int32_t* counts_out,
                    int32_t* err_count, int apply_on_input, int quant, void* a_out, float* a_scale,
                    int32_t* expert_offsets, int32_t* src2dst, int32_t* hist, cudaStream_t stream) {
@@ -404,10 +423,10 @@ int launch_scatter(const uint16_t* x, int64_t M, int K, const int32_t* ids, cons
     const size_t smem_rank = (size_t)(3 * El + 1 + (kScatterThreads / 32) * El) * sizeof(int32_t);
     int launches = 0;
     if (grid > 1) {
-        launch_k(scatter_hist_kernel, grid, kScatterThreads, (size_t)kCountCopies * El * sizeof(int32_t), stream, ids, n, expert_map, E, El, per_cta, hist, counts_in ? nullptr : err_count);
+        launch_k(scatter_hist_kernel<TId>, grid, kScatterThreads, (size_t)kCountCopies * El * sizeof(int32_t), stream, ids, n, expert_map, E, El, per_cta, hist, counts_in ? nullptr : err_count);
         ++launches;
     }
-    launch_k(scatter_rank_kernel, grid < 1 ? 1 : grid, kScatterThreads, smem_rank, stream, ids, n, expert_map, E, El, per_cta, counts_in, hist, expert_offsets, src2dst, counts_out, counts_in ? nullptr : err_count);
+    launch_k(scatter_rank_kernel<TId>, grid < 1 ? 1 : grid, kScatterThreads, smem_rank, stream, ids, n, expert_map, E, El, per_cta, counts_in, hist, expert_offsets, src2dst, counts_out, counts_in ? nullptr : err_count);
     ++launches;
     if (M > 0) {
         const int64_t warps = M * ((K + 511) / 512);
@@ -421,6 +440,13 @@ int launch_scatter(const uint16_t* x, int64_t M, int K, const int32_t* ids, cons
     note_launches(launches);
     return launch_status();
 }
+#define MOE_INSTANTIATE_SCATTER(TId)                                                                              \
+    template int launch_scatter<TId>(const uint16_t*, int64_t, int, const TId*, const float*, int, const int32_t*, \
+                                     int, int, const int32_t*, int32_t*, int32_t*, int, int, void*, float*,         \
+                                     int32_t*, int32_t*, int32_t*, cudaStream_t);
+MOE_INSTANTIATE_SCATTER(int32_t)
+MOE_INSTANTIATE_SCATTER(int64_t)
+#undef MOE_INSTANTIATE_SCATTER
 
 // ----------------------------------------------------------------------- gather
 // One warp per (token, 256-column span): lane j owns 8 bf16 columns (16 bytes). The

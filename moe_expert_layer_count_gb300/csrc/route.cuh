@@ -13,12 +13,15 @@ constexpr int kMaxLocalExperts = 1024;
 
 int scatter_slots_per_cta(int64_t n);
 
-int launch_count(const int32_t* ids, int64_t n, const int32_t* expert_map, int E, int El, int32_t* counts,
+// TId: the top-k id type, int32_t or int64_t (both instantiated in route.cu).
+template <typename TId>
+int launch_count(const TId* ids, int64_t n, const int32_t* expert_map, int E, int El, int32_t* counts,
                  int32_t* err_count, int num_sms, cudaStream_t stream);
 
 // counts_in NULL: the experts' slot counts are derived by the scatter's own histogram
 // pass and written to counts_out (bad ids then added to err_count, if not NULL).
-int launch_scatter(const uint16_t* x, int64_t M, int K, const int32_t* ids, const float* topk_weights, int topk,
+template <typename TId>
+int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const float* topk_weights, int topk,
                    const int32_t* expert_map, int E, int El, const int32_t* counts_in, int32_t* counts_out,
                    int32_t* err_count, int apply_on_input, int quant, void* a_out, float* a_scale,
                    int32_t* expert_offsets, int32_t* src2dst, int32_t* hist, cudaStream_t stream);
@@ -35,6 +38,14 @@ int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w
                         const int32_t* expert_offsets, const int32_t* expert_counts, int El, int64_t rp_cap,
                         int n_out, int k_in, int epilogue, void* out, float* out_scale, int num_sms,
                         cudaStream_t stream);
+
+// moe_forward_chunked for either top-k id type (the argument checks included).
+template <typename TId>
+int forward_chunked_impl(const void* hidden_states, const TId* topk_ids, const float* topk_weights,
+                         const uint8_t* w13, const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                         const int32_t* expert_map, int E, int local_num_experts, int64_t M, int K, int N, int topk,
+                         int64_t chunk_size, int apply_router_weight_on_input, void* out, void* workspace,
+                         size_t workspace_bytes, int32_t* err_count, cudaStream_t stream);
 
 // Device error word of the grouped GEMM (1: a pipeline wait ran out of time). Reading
 // it synchronises the device; `clear` resets it.

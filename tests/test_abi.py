@@ -68,13 +68,32 @@ def test_argument_checks_return_before_any_launch(L):
     # workspace too small
     assert L.moe_forward_chunked(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 4, 0, p,
                                  ws, 16, None, None) == 2
+    # the int64-id twins run the same checks
+    assert L.moe_count_expert_tokens_i64(p, 4, 0, None, 8, 8, p, None, None) == 1      # topk 0
+    assert L.moe_scatter_i64(p, 4, 100, p, p, 2, None, 8, 8, p, 0, None, 0, 1, p, p, p, p, 1 << 20, p,
+                             1 << 20, None) == 1                                           # K % 128
+    assert L.moe_scatter_noalloc_i64(p, 4, 128, p, p, 33, None, 8, 8, p, 0, 1, p, p, p, p, 1 << 20,
+                                     None) == 1                                            # topk > 32
+    assert L.moe_forward_chunked_i64(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 4, 0, ws,
+                                     ws, 1 << 30, None, None) == 1
+    assert L.moe_forward_host_i64(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 4, 0, p, p, 16,
+                                  None, None, None) == 2
+
+
+def test_binding_picks_the_entry_point_by_id_dtype():
+    import torch
+    import moe_expert_layer_count_gb300 as moe
+    assert moe._ids_entry("moe_scatter", torch.zeros(1, dtype=torch.int32)) == "moe_scatter"
+    assert moe._ids_entry("moe_scatter", torch.zeros(1, dtype=torch.int64)) == "moe_scatter_i64"
+    with pytest.raises(TypeError):
+        moe.moe_count_expert_tokens(torch.zeros(4, 2, dtype=torch.int16), 8, 8)
 
 
 def test_host_entry_point_checks(L):
     import moe_expert_layer_count_gb300 as moe
-    # two staging slots (x, ids, weights, out) after the layer's own workspace
+    # two staging slots (x, ids with room for int64, weights, out) after the layer's own workspace
     lay = moe.moe_workspace_size(128, 2048, 768, 8, 64)
-    slot = 128 * 2048 * 2 + 128 * 8 * 4 * 2 + 128 * 2048 * 2
+    slot = 128 * 2048 * 2 + 128 * 8 * 8 + 128 * 8 * 4 + 128 * 2048 * 2
     assert moe.moe_host_workspace_size(128, 2048, 768, 8, 64, 128) >= lay + 2 * slot
     assert moe.moe_host_workspace_size(128, 2000, 768, 8, 64, 128) == 0   # K not a multiple of 128
     assert moe.moe_host_workspace_size(0, 2048, 768, 8, 64, 128) == 0
