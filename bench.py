@@ -6,7 +6,9 @@ One step = one MoE-layer forward (count -> scatter + FP8 quant -> grouped FP8 GE
 with SiLU-and-mul requant -> grouped FP8 GEMM w2 -> gather + top-k weight-and-reduce,
 under the chunking loop) over one batch of seeded synthetic tokens already resident in
 HBM. Default workload: the Qwen3-30B-A3B-shaped layer at prefill size (M=8192 tokens,
-hidden 2048, moe intermediate 768, 128 experts, top-8, Zipf-skewed routing).
+hidden 2048, moe intermediate 768, 128 experts, top-8, Zipf-skewed routing). The timed
+steps cycle through --routings (default 5) routing batches drawn with consecutive router
+seeds, so the number averages over which experts are hot.
 
 Prints ONE JSON line (rank 0). With N > 1 (torchrun, one process per GPU) every rank
 runs its own batch (weak scaling, no data-path collective); the time is the max over
@@ -44,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--routings", type=int, default=5,
+                    help="routing batches the timed steps cycle through (router seeds seed..seed+R-1)")
     return ap.parse_args()
 
 
@@ -275,7 +279,14 @@ def run_ours(args, rank, world, local_rank):
             return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
         return torch.from_numpy(a).to(dev)
 
-    x, ids, tw = D(li.x), D(li.topk_ids), D(li.topk_weights)
+    # routing variation: timed step i runs routing batch i % R (router seeds seed .. seed+R-1,
+    # the same tokens and weights); batch 0 is the workload's own routing
+    R = max(1, args.routings)
+    host_routes = [(li.topk_ids, li.topk_weights)] + [mi.route(M, E, topk, wl.seed + b, wl.zipf_s)
+                                                      for b in range(1, R)]
+    routes = [(D(i_), D(w_)) for i_, w_ in host_routes]
+    x = D(li.x)
+    ids, tw = routes[0]
     emap = None if li.expert_map is None else D(li.expert_map)
     permute_only = N == 0
     stream = torch.cuda.current_stream()
@@ -285,8 +296,9 @@ def run_ours(args, rank, world, local_rank):
         w13, s13, w2, s2 = D(li.w13), D(li.w13_scale), D(li.w2), D(li.w2_scale)
         ws = torch.empty(moe.moe_workspace_size(cmax, K, N, topk, El), dtype=torch.uint8, device=dev)
 
-        def step():
-            moe.moe_forward_chunked(x, ids, tw, w13, s13, w2, s2, E, expert_map=emap, chunk_size=chunk,
+        def step(i=0):
+            ids_i, tw_i = routes[i % R]
+            moe.moe_forward_chunked(x, ids_i, tw_i, w13, s13, w2, s2, E, expert_map=emap, chunk_size=chunk,
                                     out=out, workspace=ws)
     else:
         cap = moe.moe_rp_cap(M, topk, El)
@@ -296,14 +308,16 @@ def run_ours(args, rank, world, local_rank):
         s2d = torch.empty(M, topk, dtype=torch.int32, device=dev)
         cnt = torch.empty(El, dtype=torch.int32, device=dev)
         sws = torch.empty(moe.moe_scatter_workspace_size(M, topk, El), dtype=torch.uint8, device=dev)
-        # identity experts: Y is the bf16 permuted copy of x
-        Y, _, _, _ = moe.moe_scatter(x, ids, tw, E, El, moe.moe_count_expert_tokens(ids, E, El, emap), emap,
-                                     quant=moe.MOE_QUANT_NONE)
+        # identity experts: Y is the bf16 permuted copy of x, one per routing batch
+        Ys = [moe.moe_scatter(x, i_, w_, E, El, moe.moe_count_expert_tokens(i_, E, El, emap), emap,
+                              quant=moe.MOE_QUANT_NONE)[0] for i_, w_ in routes]
+        Y = Ys[0]
 
-        def step():
-            moe.moe_scatter(x, ids, tw, E, El, cnt, emap, rp_cap=cap, a_out=A, a_scale=SA, expert_offsets=offs,
+        def step(i=0):
+            ids_i, tw_i = routes[i % R]
+            moe.moe_scatter(x, ids_i, tw_i, E, El, cnt, emap, rp_cap=cap, a_out=A, a_scale=SA, expert_offsets=offs,
                             src2dst=s2d, workspace=sws, count_here=True)
-            moe.moe_gather_weight_reduce(Y, s2d, tw, out=out)
+            moe.moe_gather_weight_reduce(Ys[i % R], s2d, tw_i, out=out)
 
     # per-chunk counts (host side, for the algorithmic work only)
     counts = []
@@ -316,8 +330,8 @@ def run_ours(args, rank, world, local_rank):
     clk = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
     clk.start()
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -326,8 +340,8 @@ def run_ours(args, rank, world, local_rank):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clk.mark_on()
     e0.record(stream)
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     clk.mark_off()
@@ -346,7 +360,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         layer = None if permute_only else dict(w13=w13, s13=s13, w2=w2, s2=s2, emap=emap, chunk=chunk)
-        e2e = end_to_end(moe, torch, stream, li, dev, args, step, x, ids, tw, out, layer)
+        e2e = end_to_end(moe, torch, stream, li, dev, args, step, x, routes, out, layer, host_routes)
 
     value = job_throughput(M, world, ms)
     pk = peaks()
@@ -368,6 +382,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": wl.name, "M": M, "hidden": K, "moe_intermediate": N, "experts": E,
                    "local_experts": El, "topk": topk, "chunk_size": chunk,
                    "routing": f"zipf s={wl.zipf_s}" if wl.zipf_s else "uniform",
+                   "routing_batches": f"{R} (router seeds {wl.seed}..{wl.seed + R - 1}, step i runs batch i % {R}; "
+                                      f"per-kernel breakdown and roofline on batch 0)",
                    "parallelism": f"replicas x{world} (one independent batch per GPU)",
                    "l2": "inputs larger than L2 (expert weights %.0f MB + activations)" %
                          (work.get("weight_bytes", 0) / 1e6) if not permute_only else
@@ -503,7 +519,7 @@ def roofline(kern, work, pk, wl):
 FUSED_SILU = True  # GEMM1 applies SiLU-and-mul + FP8 requant in its epilogue (as the chunk loop does)
 
 
-def end_to_end(moe, torch, stream, li, dev, args, step_dev, x, ids, tw, out, layer):
+def end_to_end(moe, torch, stream, li, dev, args, step_dev, x, routes, out, layer, host_routes):
     """Same metric through the public API with host buffers: every step copies that
     step's inputs from pinned host memory to the device and the output back.
 
@@ -515,8 +531,10 @@ def end_to_end(moe, torch, stream, li, dev, args, step_dev, x, ids, tw, out, lay
     calls on the compute stream."""
     wl = li.wl
     xh = torch.from_numpy(np.ascontiguousarray(li.x).view(np.int16)).view(torch.bfloat16).pin_memory()
-    ih = torch.from_numpy(np.ascontiguousarray(li.topk_ids)).pin_memory()
-    wh = torch.from_numpy(np.ascontiguousarray(li.topk_weights)).pin_memory()
+    ihs = [torch.from_numpy(np.ascontiguousarray(i_)).pin_memory() for i_, _ in host_routes]
+    whs = [torch.from_numpy(np.ascontiguousarray(w_)).pin_memory() for _, w_ in host_routes]
+    ih, wh = ihs[0], whs[0]
+    R = len(host_routes)
     oh = [torch.empty(wl.M, wl.K, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     if layer is not None:
         El, N2, _ = layer["w13"].shape
@@ -524,7 +542,8 @@ def end_to_end(moe, torch, stream, li, dev, args, step_dev, x, ids, tw, out, lay
                           dtype=torch.uint8, device=dev)
 
         def step(i):
-            moe.moe_forward_host(xh, ih, wh, layer["w13"], layer["s13"], layer["w2"], layer["s2"], wl.E,
+            moe.moe_forward_host(xh, ihs[i % R], whs[i % R], layer["w13"], layer["s13"], layer["w2"], layer["s2"],
+                                 wl.E,
                                  expert_map=layer["emap"], chunk_size=layer["chunk"], out=oh[i & 1],
                                  workspace=hws, stream=stream)
 
@@ -532,10 +551,11 @@ def end_to_end(moe, torch, stream, li, dev, args, step_dev, x, ids, tw, out, lay
             moe.moe_host_wait(stream)
     else:
         def step(i):
+            ids_i, tw_i = routes[i % R]
             x.copy_(xh, non_blocking=True)
-            ids.copy_(ih, non_blocking=True)
-            tw.copy_(wh, non_blocking=True)
-            step_dev()
+            ids_i.copy_(ihs[i % R], non_blocking=True)
+            tw_i.copy_(whs[i % R], non_blocking=True)
+            step_dev(i)
             oh[i & 1].copy_(out, non_blocking=True)
 
         def drain():
