@@ -123,6 +123,16 @@ template int launch_count<int64_t>(const int64_t*, int64_t, const int32_t*, int,
 
 constexpr int kRound = 8;  // groups of 32 slots loaded per warp per round
 
+// A 16-byte load of data this kernel reads exactly once and that nothing writes while it
+// runs: no L1 allocation, and 256-byte L2 fetches (a warp reads 512 contiguous bytes).
+__device__ __forceinline__ uint4 ld_once_256(const void* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
 int scatter_slots_per_cta(int64_t n) {
     constexpr int64_t kUnit = (kScatterThreads / 32) * 32;  // 32 slots for each warp
     int64_t per = (n + kMaxScatterCtas - 1) / kMaxScatterCtas;
@@ -452,6 +462,8 @@ MOE_INSTANTIATE_SCATTER(int64_t)
 // One warp per (token, 256-column span): lane j owns 8 bf16 columns (16 bytes). The
 // kept rows of the token are loaded 8 at a time (independent 16-byte loads in flight),
 // then accumulated in ascending k with separately rounded fp32 multiply and add.
+// Y is read exactly once (ld_once_256).
+
 __global__ void __launch_bounds__(256)
     gather_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ src2dst,
                   const float* __restrict__ topk_weights, int64_t M, int topk, int K, int apply_on_input,
@@ -478,7 +490,7 @@ __global__ void __launch_bounds__(256)
             d[j] = __shfl_sync(0xffffffffu, my_dst, (k0 + j) & 31);
             if (k0 + j >= topk) d[j] = -1;
             r[j] = make_uint4(0, 0, 0, 0);
-            if (d[j] >= 0 && active) r[j] = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)d[j] * K + col));
+            if (d[j] >= 0 && active) r[j] = ld_once_256(y + (int64_t)d[j] * K + col);
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
