@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each step from a CUDA graph captured once per routing batch")
     ap.add_argument("--routings", type=int, default=5,
                     help="routing batches the timed steps cycle through (router seeds seed..seed+R-1)")
     return ap.parse_args()
@@ -329,9 +331,30 @@ def run_ours(args, rank, world, local_rank):
 
     clk = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
+    run = step
+    graph_launches = None
+    if args.graph:
+        # one CUDA graph per routing batch, captured on the same static buffers the eager
+        # steps use; a replay launches the step's kernels without the host API in between
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for i in range(R):
+                step(i)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        lc0 = moe.moe_kernel_launch_count()
+        graphs = []
+        for b in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(b)
+            graphs.append(g)
+        graph_launches = (moe.moe_kernel_launch_count() - lc0) // R  # kernels in one step's graph
+        run = lambda i: graphs[i % R].replay()
     clk.start()
     for i in range(args.warmup):
-        step(i)
+        run(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -341,11 +364,11 @@ def run_ours(args, rank, world, local_rank):
     clk.mark_on()
     e0.record(stream)
     for i in range(args.steps):
-        step(i)
+        run(i)
     e1.record(stream)
     torch.cuda.synchronize()
     clk.mark_off()
-    launches = (moe.moe_kernel_launch_count() - l0)
+    launches = (moe.moe_kernel_launch_count() - l0) if graph_launches is None else graph_launches * args.steps
     ms = e0.elapsed_time(e1) / args.steps
     if world > 1:
         dist.barrier()
@@ -382,6 +405,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": wl.name, "M": M, "hidden": K, "moe_intermediate": N, "experts": E,
                    "local_experts": El, "topk": topk, "chunk_size": chunk,
                    "routing": f"zipf s={wl.zipf_s}" if wl.zipf_s else "uniform",
+                   "cuda_graph": bool(args.graph),
                    "routing_batches": f"{R} (router seeds {wl.seed}..{wl.seed + R - 1}, step i runs batch i % {R}; "
                                       f"per-kernel breakdown and roofline on batch 0)",
                    "parallelism": f"replicas x{world} (one independent batch per GPU)",
