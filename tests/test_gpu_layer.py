@@ -242,6 +242,19 @@ def test_layer_interface_extremes(E, topk, local, chunk):
     layer_tolerance(got, ref)
 
 
+@pytest.mark.parametrize("K,N,E,topk,M", [(7168, 256, 8, 2, 40),    # a wide hidden size: 56 K blocks in GEMM1
+                                           (512, 2048, 4, 2, 40),     # a wide expert: 16 K blocks in GEMM2
+                                           (4096, 1408, 6, 2, 30)])   # 2N = 2816: an odd count of 256-wide tiles
+def test_layer_other_model_shapes(K, N, E, topk, M):
+    """Hidden and expert sizes of other MoE models (long K loops wrap the pipeline's
+    stage and TMEM-buffer phases many times per tile), against the oracle."""
+    wl = mi.Workload(f"shape_k{K}_n{N}", M=M, K=K, N=N, E=E, topk=topk, seed=K + N, zipf_s=1.2)
+    li = mi.make_layer_inputs(wl)
+    got = gpu_forward(to_dev_layer(li), E)
+    ref = oracle_forward(li)
+    layer_tolerance(got, ref)
+
+
 def random_layer_case(seed):
     """A seeded random layer configuration: sizes, expert count, top-k, a random local
     expert map (or none), chunking, routing skew and where the router weight applies."""
