@@ -105,3 +105,50 @@ def test_host_entry_point_checks(L):
                               None, None, None) == 2                                   # workspace too small
     assert L.moe_forward_host(p, p, p, p, p, p, p, None, 8, 8, 0, 128, 128, 2, 4, 0, p, p, 16,
                               None, None, None) == 0                                   # M = 0: no-op
+
+
+def test_every_entry_point_refuses_bad_arguments_on_the_host(L):
+    """Each documented argument error returns its status before anything is enqueued
+    (no device is touched: these calls run on a machine without a GPU)."""
+    p, odd = ctypes.c_void_p(16), ctypes.c_void_p(8)  # 16-byte aligned / misaligned
+    INVALID, SMALL, SCRATCH = 1, 2, 5
+    # count: E < 1, top-k > 32, ids missing for M > 0
+    assert L.moe_count_expert_tokens(p, 4, 2, None, 0, 1, p, None, None) == INVALID
+    assert L.moe_count_expert_tokens(p, 4, 33, None, 64, 64, p, None, None) == INVALID
+    assert L.moe_count_expert_tokens(None, 4, 2, None, 8, 8, p, None, None) == INVALID
+
+    def scatter(M=4, K=128, topk=2, El=8, quant=1, x=p, rp_cap=1 << 20, ws_bytes=1 << 20, fn=L.moe_scatter):
+        return fn(x, M, K, p, p, topk, None, 8, El, p, 0, None, 0, quant, p, p, p, p, rp_cap, p, ws_bytes, None)
+    assert scatter(K=100) == INVALID                                 # K not a multiple of 128
+    assert scatter(quant=7) == INVALID                               # unknown quantisation
+    assert scatter(x=odd) == INVALID                                 # rows not 16-byte aligned
+    assert scatter(rp_cap=L.moe_rp_cap(4, 2, 8) - 128) == INVALID    # row bound below moe_rp_cap
+    assert scatter(M=1000, topk=8, ws_bytes=16) == SMALL             # many blocks, scratch too small
+    assert scatter(K=100, fn=L.moe_scatter_i64) == INVALID
+    # allocation-free scatter: more block histograms than its fixed scratch holds
+    M, topk, El = 100000, 8, 1024
+    assert L.moe_scatter_noalloc(p, M, 128, p, p, topk, None, El, El, p, 0, 1, p, p, p, p,
+                                 L.moe_rp_cap(M, topk, El), None) == SCRATCH
+
+    def gemm(El=4, rp_cap=256, n_out=256, k_in=256, epi=0, out=p):
+        return L.moe_grouped_gemm_fp8(p, p, p, p, p, None, El, rp_cap, n_out, k_in, epi, out, p, None)
+    assert gemm(epi=9) == INVALID                                    # unknown epilogue
+    assert gemm(n_out=200) == INVALID                                # n_out not a multiple of 128
+    assert gemm(rp_cap=200) == INVALID                               # row bound not a multiple of 128
+    assert gemm(El=2000) == INVALID                                  # more than 1024 local experts
+    assert gemm(out=odd) == INVALID                                  # output not 16-byte aligned
+    # standalone SiLU-and-mul: N not a multiple of 128, misaligned input
+    assert L.moe_silu_mul_quant(p, p, 4, 128, 100, p, p, None) == INVALID
+    assert L.moe_silu_mul_quant(odd, p, 4, 128, 128, p, p, None) == INVALID
+    # gather: top-k > 32, negative M, weights missing when they are applied here
+    assert L.moe_gather_weight_reduce(p, p, p, 4, 33, 128, 0, p, None) == INVALID
+    assert L.moe_gather_weight_reduce(p, p, p, -1, 2, 128, 0, p, None) == INVALID
+    assert L.moe_gather_weight_reduce(p, p, None, 4, 2, 128, 0, p, None) == INVALID
+    # whole layer: chunk size < 1, N not a multiple of 128; M = 0 is a no-op
+    ws = ctypes.c_void_p(1 << 20)
+    assert L.moe_forward_chunked(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 0, 0, p, ws, 1 << 30,
+                                 None, None) == INVALID
+    assert L.moe_forward_chunked(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 100, 2, 4, 0, p, ws, 1 << 30,
+                                 None, None) == INVALID
+    assert L.moe_forward_chunked(p, p, p, p, p, p, p, None, 8, 8, 0, 128, 128, 2, 4, 0, p, ws, 1 << 30,
+                                 None, None) == 0
