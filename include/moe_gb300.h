@@ -27,7 +27,9 @@
  *  - Row-major layouts throughout. bf16 is IEEE bfloat16 (2 bytes); fp8 is OCP E4M3
  *    ("float8_e4m3fn", 1 byte); scales are fp32.
  *  - K (hidden) and N (intermediate) are multiples of 128; 1 <= topk <= 32;
- *    1 <= local_num_experts <= 1024; 1 <= E.
+ *    1 <= local_num_experts <= 1024; 1 <= E. Row indices (src2dst, expert_offsets,
+ *    counts) are int32, so M * topk and the permuted row count rp_cap must not exceed
+ *    2^31 - 1 (MOE_ERR_INVALID_ARG otherwise).
  *  - Local expert of a top-k slot: l = expert_map ? expert_map[id] : id. The slot is
  *    kept when 0 <= l < local_num_experts. An id of -1 is an empty slot and is dropped
  *    silently; any other id outside [0, E) is dropped and counted in *err_count (when
@@ -176,7 +178,10 @@ MOE_API int moe_scatter_i64(const void* hidden_states, int64_t M, int K, const i
  * 131k top-k slots at 1024 local experts or about 16.7M slots at 128 -- is refused with
  * MOE_ERR_SCRATCH_LIMIT before anything is enqueued.
  * The first call on each device looks up the array's device address (with that device
- * current); make that first call before any stream capture. Every call on a device
+ * current); make that first call before any stream capture. The address is kept for the
+ * life of the process, so this entry point must not be called on a device after
+ * cudaDeviceReset (or any other teardown of its primary context) in the same process:
+ * the array then moves and the kept address is stale. Every call on a device
  * shares the one array and overwrites the entries it reads, so calls whose kernels
  * overlap on the GPU (different streams, no ordering between them) race and give wrong
  * results: order them on one stream or with events. Allocates nothing. */
@@ -293,7 +298,11 @@ MOE_API size_t moe_host_workspace_size(int64_t M, int K, int N, int topk, int lo
  * next call's layer. out_host holds the result once `done` (a cudaEvent_t, or NULL) has
  * completed, or once `stream` has passed a later moe_host_wait. The host buffers must
  * stay untouched until then. `stream` itself is NOT ordered after the output copy.
- * Calls that share a workspace must use the same `stream`.
+ * Calls that share a workspace must use the same `stream`. Batches of different sizes may
+ * share one workspace (sized for the largest): a call whose M, chunk_size or workspace
+ * differs from the previous call's places its staging slots differently, so its input
+ * copy first waits for every earlier call's layer and output copies; only calls of one
+ * size overlap one another.
  * workspace >= moe_host_workspace_size(M, K, N, topk, El, chunk_size) bytes. */
 MOE_API int moe_forward_host(const void* hidden_states_host, const int32_t* topk_ids_host,
                              const float* topk_weights_host, const uint8_t* w13, const float* w13_scale,

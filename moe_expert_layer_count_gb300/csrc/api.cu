@@ -2,6 +2,7 @@
 // chunking loop. Every computation is enqueued as a kernel on the caller's stream;
 // nothing here allocates, frees or synchronises.
 #include <atomic>
+#include <climits>
 
 #include "common.cuh"
 #include "route.cuh"
@@ -40,7 +41,9 @@ int check_device(int* num_sms) {
 inline size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 bool routing_args_ok(int64_t M, int topk, int E, int El) {
-    return M >= 0 && topk >= 1 && topk <= 32 && E >= 1 && El >= 1 && El <= kMaxLocalExperts;
+    // slots and permuted rows are indexed with int32 (src2dst, offsets, counts)
+    return M >= 0 && topk >= 1 && topk <= 32 && E >= 1 && El >= 1 && El <= kMaxLocalExperts &&
+           M <= INT32_MAX / topk && moe_rp_cap(M, topk, El) <= INT32_MAX;
 }
 
 // Byte layout of the chunk workspace (offsets from its base, each 256-aligned):
@@ -148,7 +151,7 @@ int scatter_impl(const void* hidden_states, int64_t M, int K, const TId* topk_id
         return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(hidden_states) | reinterpret_cast<uintptr_t>(a_out)) & 15)
         return MOE_ERR_INVALID_ARG;
-    if (rp_cap < moe_rp_cap(M, topk, local_num_experts)) return MOE_ERR_INVALID_ARG;
+    if (rp_cap < moe_rp_cap(M, topk, local_num_experts) || rp_cap > INT32_MAX) return MOE_ERR_INVALID_ARG;
     const size_t need = moe_scatter_workspace_size(M, topk, local_num_experts);
     const int64_t per = scatter_slots_per_cta(M * topk);
     const bool multi = (M * topk + per - 1) / per > 1;
@@ -158,7 +161,7 @@ int scatter_impl(const void* hidden_states, int64_t M, int K, const TId* topk_id
                           local_num_experts, count_here ? nullptr : expert_num_tokens,
                           count_here ? expert_num_tokens : nullptr, count_here ? err_count : nullptr,
                           apply_router_weight_on_input ? 1 : 0, quant, a_out, a_scale, expert_offsets, src2dst,
-                          static_cast<int32_t*>(workspace), (cudaStream_t)stream);
+                          rp_cap, static_cast<int32_t*>(workspace), (cudaStream_t)stream);
 }
 
 }  // namespace
@@ -205,7 +208,7 @@ MOE_API int moe_grouped_gemm_fp8(const uint8_t* a, const float* a_scale, const u
                                  int local_num_experts, int64_t rp_cap, int n_out, int k_in, int epilogue, void* out,
                                  float* out_scale, moe_stream_t stream) {
     if (!a || !a_scale || !w || !w_scale || !expert_offsets || !out || local_num_experts < 1 ||
-        local_num_experts > kMaxLocalExperts || rp_cap < 0 || rp_cap % kGroup || n_out <= 0 || k_in <= 0 ||
+        local_num_experts > kMaxLocalExperts || rp_cap < 0 || rp_cap > INT32_MAX || rp_cap % kGroup || n_out <= 0 || k_in <= 0 ||
         n_out % kGroup || k_in % kGroup)
         return MOE_ERR_INVALID_ARG;
     if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_F32 && epilogue != MOE_EPI_SILU_MUL_QUANT)
@@ -221,7 +224,8 @@ MOE_API int moe_grouped_gemm_fp8(const uint8_t* a, const float* a_scale, const u
 
 MOE_API int moe_silu_mul_quant(const float* c1, const int32_t* expert_offsets, int local_num_experts, int64_t rp_cap,
                                int N, uint8_t* h, float* h_scale, moe_stream_t stream) {
-    if (!c1 || !expert_offsets || !h || !h_scale || local_num_experts < 1 || rp_cap < 0 || N <= 0 || N % kGroup)
+    if (!c1 || !expert_offsets || !h || !h_scale || local_num_experts < 1 || rp_cap < 0 || rp_cap > INT32_MAX ||
+        N <= 0 || N % kGroup)
         return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(c1) | reinterpret_cast<uintptr_t>(h)) & 15) return MOE_ERR_INVALID_ARG;
     if (int st = check_device(nullptr)) return st;
@@ -231,7 +235,7 @@ MOE_API int moe_silu_mul_quant(const float* c1, const int32_t* expert_offsets, i
 MOE_API int moe_gather_weight_reduce(const void* y, const int32_t* src2dst, const float* topk_weights, int64_t M,
                                      int topk, int K, int apply_router_weight_on_input, void* out,
                                      moe_stream_t stream) {
-    if (M < 0 || topk < 1 || topk > 32 || K <= 0 || K % kGroup) return MOE_ERR_INVALID_ARG;
+    if (M < 0 || topk < 1 || topk > 32 || M > INT32_MAX / topk || K <= 0 || K % kGroup) return MOE_ERR_INVALID_ARG;
     if (M > 0 && (!y || !src2dst || !out || (!apply_router_weight_on_input && !topk_weights)))
         return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(out)) & 15) return MOE_ERR_INVALID_ARG;
@@ -315,7 +319,7 @@ int forward_chunked_impl(const void* hidden_states, const TId* topk_ids, const f
         const float* tw = topk_weights + c0 * topk;
         // the chunk's expert counts come out of the scatter's own histogram pass
         int st = launch_scatter(x + c0 * K, Mc, K, ids, tw, topk, expert_map, E, El, nullptr, counts, err_count,
-                                apply_router_weight_on_input ? 1 : 0, MOE_QUANT_FP8_1X128, A, sa, offs, s2d, hist, s);
+                                apply_router_weight_on_input ? 1 : 0, MOE_QUANT_FP8_1X128, A, sa, offs, s2d, cap, hist, s);
         if (!st)
             st = launch_grouped_gemm(A, sa, w13, w13_scale, offs, counts, El, cap, 2 * N, K, MOE_EPI_SILU_MUL_QUANT, H, sh,
                                      sms, s);

@@ -34,6 +34,7 @@
 // named barrier of the tile it leaves, so the exchange never waits for it.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -52,6 +53,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kScaleWarp = 10;
+constexpr int kMaxDevices = 64;
 
 // Whether an epilogue gets its block scales from the scale warp's ring, and the block
 // size that follows (at most 3 warps per SM sub-partition either way).
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, const float* __restrict__ sa, const float* __restrict__ sw,
                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts,
-                   int El, int n_out, int k_in, void* __restrict__ out, float* __restrict__ out_scale) {
+                   int El, int row_cap, int n_out, int k_in, void* __restrict__ out, float* __restrict__ out_scale) {
     using C = Cfg<BN, EPI>;
     constexpr bool kSilu = EPI == MOE_EPI_SILU_MUL_QUANT;
     constexpr bool kStaged = staged_scales<EPI>();
@@ -225,7 +227,8 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
     ptx::tc_fence_after();
     const uint32_t tmem = st->tmem_base;
 
-    const int m_tiles = s_off[El] / kBM;
+    // rows past the buffers' row count are never touched, whatever the offsets say
+    const int m_tiles = min(s_off[El], row_cap) / kBM;
     const int n_tiles = kSilu ? n_out / 256 : n_out / BN;
     const int tiles = m_tiles * n_tiles;
     const int KB = k_in / kBK;
@@ -605,19 +608,23 @@ int launch_tc_k(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
                 const float* w_scale, const int32_t* offsets, const int32_t* counts, int El, int64_t rp_cap,
                 int n_out, int k_in, void* out, float* out_scale, int num_sms, cudaStream_t stream) {
     const size_t smem = smem_bytes<BN, EPI>(El);
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, kSkip>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)smem_bytes<BN, EPI>(kMaxLocalExperts));
-    });
-    if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+    // the shared-memory opt-in is a property of the kernel in each device's context: set
+    // it once per device (racing first calls only set the same value twice)
+    static std::atomic<bool> attr_set[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, kSkip>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes<BN, EPI>(kMaxLocalExperts)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set[dev].store(true, std::memory_order_release);
+    }
     const int n_tiles = EPI == MOE_EPI_SILU_MUL_QUANT ? n_out / 256 : n_out / BN;
     const int64_t max_tiles = rp_cap / kBM * n_tiles;
     const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid < 1) return MOE_OK;
     launch_k(gemm_tc_kernel<BN, EPI, kSkip>, grid, threads_of<EPI>(), smem, stream, ta, tb, to, a_scale, w_scale,
-             offsets, counts, El, n_out, k_in, out, out_scale);
+             offsets, counts, El, (int)rp_cap, n_out, k_in, out, out_scale);
     note_launches(1);
     return launch_status();
 }

@@ -32,6 +32,11 @@ struct HostPipe {
     unsigned calls = 0;
     int last = -1;  // slot of the most recent call
     bool ready = false;
+    // Placement of the previous call's layer area and slots. A call of another size (or
+    // on another workspace) places them differently, so its regions can overlap bytes
+    // that earlier calls' kernels and copies are still using.
+    const void* ws = nullptr;
+    size_t layer_bytes = 0, slot_bytes = 0;
 };
 
 std::mutex g_pipe_mutex[kMaxDevices];
@@ -119,6 +124,15 @@ int forward_host_impl(const void* hidden_states_host, const TId* topk_ids_host, 
     void* out = base + L.out;
     cudaStream_t cs = (cudaStream_t)stream;
 
+    // A new placement drains the pipeline first: the input copy waits for every earlier
+    // call's layer and both slots' output copies (an event never recorded is complete).
+    // Calls of one size keep overlapping.
+    if (p.calls && (p.ws != workspace || p.layer_bytes != layer_bytes || p.slot_bytes != L.total)) {
+        if (cudaStreamWaitEvent(p.h2d, p.compute_done[p.last], 0) != cudaSuccess ||
+            cudaStreamWaitEvent(p.h2d, p.out_done[0], 0) != cudaSuccess ||
+            cudaStreamWaitEvent(p.h2d, p.out_done[1], 0) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     // inputs into the slot, once its previous use has been copied out
     if (cudaStreamWaitEvent(p.h2d, p.out_done[s], 0) != cudaSuccess ||
         cudaMemcpyAsync(x, hidden_states_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, p.h2d) != cudaSuccess ||
@@ -140,6 +154,9 @@ int forward_host_impl(const void* hidden_states_host, const TId* topk_ids_host, 
         return MOE_ERR_CUDA;
     if (done && cudaEventRecord((cudaEvent_t)done, p.d2h) != cudaSuccess) return MOE_ERR_CUDA;
     p.last = s;
+    p.ws = workspace;
+    p.layer_bytes = layer_bytes;
+    p.slot_bytes = L.total;
     ++p.calls;
     return MOE_OK;
 }

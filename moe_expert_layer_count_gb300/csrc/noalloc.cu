@@ -8,6 +8,7 @@
 // buffers. For them this entry point keeps the scratch in a fixed-size array that lives
 // in the library's own device memory, so the call itself allocates nothing.
 #include <atomic>
+#include <climits>
 
 #include "common.cuh"
 #include "route.cuh"
@@ -24,7 +25,9 @@ constexpr int kMaxDevices = 64;
 std::atomic<int32_t*> g_scratch_ptr[kMaxDevices];
 
 // Device address of g_scatter_scratch on the current device, looked up once per device
-// (the first call on each device does it, with that device current).
+// (the first call on each device does it, with that device current) and kept for the
+// life of the process: a device reset would reload the module elsewhere, which is why
+// the header rules out calls after one.
 int scratch_address(int32_t** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -47,7 +50,7 @@ int scatter_noalloc_impl(const void* hidden_states, int64_t M, int K, const TId*
                          float* a_scale, int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap,
                          moe_stream_t stream) {
     if (M < 0 || topk < 1 || topk > 32 || E < 1 || local_num_experts < 1 || local_num_experts > kMaxLocalExperts ||
-        K <= 0 || K % kGroup || !expert_num_tokens || !expert_offsets ||
+        M > INT32_MAX / topk || K <= 0 || K % kGroup || !expert_num_tokens || !expert_offsets ||
         (quant != MOE_QUANT_NONE && quant != MOE_QUANT_FP8_1X128))
         return MOE_ERR_INVALID_ARG;
     if (M > 0 && (!hidden_states || !topk_ids || !src2dst || !a_out || (quant == MOE_QUANT_FP8_1X128 && !a_scale) ||
@@ -55,7 +58,7 @@ int scatter_noalloc_impl(const void* hidden_states, int64_t M, int K, const TId*
         return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(hidden_states) | reinterpret_cast<uintptr_t>(a_out)) & 15)
         return MOE_ERR_INVALID_ARG;
-    if (rp_cap < moe_rp_cap(M, topk, local_num_experts)) return MOE_ERR_INVALID_ARG;
+    if (rp_cap < moe_rp_cap(M, topk, local_num_experts) || rp_cap > INT32_MAX) return MOE_ERR_INVALID_ARG;
     // the histograms of all blocks must fit the fixed scratch
     const int64_t n = M * topk;
     const int64_t per = scatter_slots_per_cta(n);
@@ -73,8 +76,8 @@ int scatter_noalloc_impl(const void* hidden_states, int64_t M, int K, const TId*
     // previous call's contents never leak into this one
     return launch_scatter(static_cast<const uint16_t*>(hidden_states), M, K, topk_ids, topk_weights, topk, expert_map,
                           E, local_num_experts, expert_num_tokens, nullptr, nullptr,
-                          apply_router_weight_on_input ? 1 : 0, quant, a_out, a_scale, expert_offsets, src2dst, scratch,
-                          (cudaStream_t)stream);
+                          apply_router_weight_on_input ? 1 : 0, quant, a_out, a_scale, expert_offsets, src2dst, rp_cap,
+                          scratch, (cudaStream_t)stream);
 }
 
 }  // namespace

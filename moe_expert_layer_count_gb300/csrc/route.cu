@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kScatterThreads)
     scatter_rank_kernel(const TId* __restrict__ ids, int64_t n, const int32_t* __restrict__ expert_map, int E,
                         int El, int per_cta, const int32_t* __restrict__ counts_in, const int32_t* __restrict__ hist,
                         int32_t* __restrict__ expert_offsets, int32_t* __restrict__ src2dst,
-                        int32_t* __restrict__ counts_out, int32_t* __restrict__ err_count) {
+                        int32_t* __restrict__ counts_out, int32_t* __restrict__ err_count, int row_cap) {
     constexpr int kWarps = kScatterThreads / 32;
     extern __shared__ int32_t sm[];
     int32_t* off = sm;               // [El + 1]
@@ -286,6 +286,9 @@ __global__ void __launch_bounds__(kScatterThreads)
     }
     __syncthreads();
     if (warp == 0) {  // exclusive scan of the padded block sizes
+        // Offsets never pass the caller's row bound (a multiple of 128): counts given by
+        // the caller that disagree with the ids cannot place rows outside a_out. With
+        // consistent counts the bound is never reached.
         int run = 0;
         for (int lb = 0; lb < El; lb += 32) {
             const int l = lb + lane;
@@ -296,8 +299,8 @@ __global__ void __launch_bounds__(kScatterThreads)
                 const int t = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += t;
             }
-            if (l < El) off[l] = run + incl - c;
-            run += __shfl_sync(0xffffffffu, incl, 31);
+            if (l < El) off[l] = min(run + incl - c, row_cap);
+            run = min(run + __shfl_sync(0xffffffffu, incl, 31), row_cap);
         }
         if (lane == 0) off[El] = run;
     }
@@ -329,7 +332,9 @@ __global__ void __launch_bounds__(kScatterThreads)
             dst[j] = -1;
             if (l[j] >= 0) {
                 dst[j] = mine[l[j]] + rank;
-                if (dst[j] >= off[l[j] + 1]) dst[j] = -1;  // counts inconsistent with ids: drop, never overflow
+                // counts inconsistent with the ids: the slot is dropped, never written past
+                // its expert's block (whose end is at most the row bound)
+                if (dst[j] >= off[l[j] + 1]) dst[j] = -1;
             }
             __syncwarp();
             if (l[j] >= 0 && rank == 0) mine[l[j]] += __popc(m);
@@ -426,8 +431,9 @@ template <typename TId>
 int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const float* topk_weights, int topk,
                    const int32_t* expert_map, int E, int El, const int32_t* counts_in, int32_t* counts_out,
                    int32_t* err_count, int apply_on_input, int quant, void* a_out, float* a_scale,
-                   int32_t* expert_offsets, int32_t* src2dst, int32_t* hist, cudaStream_t stream) {
+                   int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, int32_t* hist, cudaStream_t stream) {
     const int64_t n = M * topk;
+    const int row_cap = (int)(rp_cap / kGroup * kGroup);
     const int per_cta = scatter_slots_per_cta(n);
     const int grid = (int)((n + per_cta - 1) / per_cta);
     const size_t smem_rank = (size_t)(3 * El + 1 + (kScatterThreads / 32) * El) * sizeof(int32_t);
@@ -436,7 +442,7 @@ int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const fl
         launch_k(scatter_hist_kernel<TId>, grid, kScatterThreads, (size_t)kCountCopies * El * sizeof(int32_t), stream, ids, n, expert_map, E, El, per_cta, hist, counts_in ? nullptr : err_count);
         ++launches;
     }
-    launch_k(scatter_rank_kernel<TId>, grid < 1 ? 1 : grid, kScatterThreads, smem_rank, stream, ids, n, expert_map, E, El, per_cta, counts_in, hist, expert_offsets, src2dst, counts_out, counts_in ? nullptr : err_count);
+    launch_k(scatter_rank_kernel<TId>, grid < 1 ? 1 : grid, kScatterThreads, smem_rank, stream, ids, n, expert_map, E, El, per_cta, counts_in, hist, expert_offsets, src2dst, counts_out, counts_in ? nullptr : err_count, row_cap);
     ++launches;
     if (M > 0) {
         const int64_t warps = M * ((K + 511) / 512);
@@ -453,7 +459,7 @@ int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const fl
 #define MOE_INSTANTIATE_SCATTER(TId)                                                                              \
     template int launch_scatter<TId>(const uint16_t*, int64_t, int, const TId*, const float*, int, const int32_t*, \
                                      int, int, const int32_t*, int32_t*, int32_t*, int, int, void*, float*,         \
-                                     int32_t*, int32_t*, int32_t*, cudaStream_t);
+                                     int32_t*, int32_t*, int64_t, int32_t*, cudaStream_t);
 MOE_INSTANTIATE_SCATTER(int32_t)
 MOE_INSTANTIATE_SCATTER(int64_t)
 #undef MOE_INSTANTIATE_SCATTER

@@ -152,3 +152,29 @@ def test_every_entry_point_refuses_bad_arguments_on_the_host(L):
                                  None, None) == INVALID
     assert L.moe_forward_chunked(p, p, p, p, p, p, p, None, 8, 8, 0, 128, 128, 2, 4, 0, p, ws, 1 << 30,
                                  None, None) == 0
+
+
+def test_int32_row_indices_bound_the_sizes(L):
+    """Slots and permuted rows are indexed with int32: sizes that would overflow them are
+    refused on the host, by every entry point that builds such indices."""
+    p = ctypes.c_void_p(16)
+    INVALID = 1
+    big_M = (1 << 31) // 8 + 1                      # M * top-8 > 2^31 - 1
+    assert L.moe_count_expert_tokens(p, big_M, 8, None, 128, 128, p, None, None) == INVALID
+    assert L.moe_count_expert_tokens_i64(p, big_M, 8, None, 128, 128, p, None, None) == INVALID
+    assert L.moe_scatter(p, big_M, 128, p, p, 8, None, 128, 128, p, 0, None, 0, 1, p, p, p, p, 1 << 40, p,
+                         1 << 40, None) == INVALID
+    assert L.moe_scatter_noalloc(p, big_M, 128, p, p, 8, None, 128, 128, p, 0, 1, p, p, p, p, 1 << 40,
+                                 None) == INVALID
+    assert L.moe_gather_weight_reduce(p, p, p, big_M, 8, 128, 0, p, None) == INVALID
+    assert L.moe_workspace_size(big_M, 128, 128, 8, 128) == 0
+    # M * topk fits, but the padded row bound does not
+    M = (1 << 31) // 8 - 1000
+    assert L.moe_rp_cap(M, 8, 1024) > (1 << 31) - 1
+    assert L.moe_count_expert_tokens(p, M, 8, None, 1024, 1024, p, None, None) == INVALID
+    # a row bound past int32 on the GEMM and the standalone SiLU
+    assert L.moe_grouped_gemm_fp8(p, p, p, p, p, None, 4, 1 << 31, 256, 256, 0, p, p, None) == INVALID
+    assert L.moe_silu_mul_quant(p, p, 4, 1 << 31, 128, p, p, None) == INVALID
+    # the scatter's own row bound must stay in int32 too
+    assert L.moe_scatter(p, 4, 128, p, p, 2, None, 8, 8, p, 0, None, 0, 1, p, p, p, p, 1 << 31, p, 1 << 20,
+                         None) == INVALID

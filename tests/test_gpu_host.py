@@ -80,3 +80,39 @@ def test_forward_host_needs_pinned_host_tensors():
             pinned(li.topk_weights), dev(li.w13), dev(li.w13_scale), dev(li.w2), dev(li.w2_scale), mi.TINY.E)
     with pytest.raises(ValueError):
         moe.moe_forward_host(*args)  # hidden_states is pageable
+
+
+def test_forward_host_interleaved_sizes_share_one_workspace():
+    """Large and small batches alternate on one workspace sized for the largest, several
+    calls in flight: a call whose size differs from the previous one places its staging
+    slots elsewhere, and must not overwrite bytes an earlier call is still using."""
+    wl = mi.QWEN3_DECODE
+    li = mi.make_layer_inputs(wl)
+    K, E, topk = wl.K, wl.E, wl.topk
+    El, N2, _ = li.w13.shape
+    w = dict(w13=dev(li.w13), s13=dev(li.w13_scale), w2=dev(li.w2), s2=dev(li.w2_scale))
+    sizes = [2048, 64, 2048, 7, 1500, 2048, 1, 2048, 640]
+    chunk = 512
+    bs = []
+    for i, M in enumerate(sizes):
+        ids, tw = mi.route(M, E, topk, 100 + i, 1.2)
+        bs.append((mi.hidden_states(M, K, 100 + i), ids, tw))
+    refs = []
+    for x, ids, tw in bs:
+        out = moe.moe_forward_chunked(dev(x), dev(ids), dev(tw), w["w13"], w["s13"], w["w2"], w["s2"], E,
+                                      chunk_size=chunk)
+        torch.cuda.synchronize()
+        refs.append(host_bits(out))
+    ws = torch.empty(moe.moe_host_workspace_size(max(sizes), K, N2 // 2, topk, El, chunk), dtype=torch.uint8,
+                     device="cuda")
+    hin = [tuple(pinned(a) for a in b) for b in bs]
+    outs, evs = [], []
+    for x, ids, tw in hin:  # all calls in flight before any wait
+        ev = torch.cuda.Event()
+        outs.append(moe.moe_forward_host(x, ids, tw, w["w13"], w["s13"], w["w2"], w["s2"], E, chunk_size=chunk,
+                                         workspace=ws, done=ev))
+        evs.append(ev)
+    for ev in evs:
+        ev.synchronize()
+    for i, (got, ref) in enumerate(zip(outs, refs)):
+        assert (got.view(torch.int16).numpy().view(np.uint16) == ref).all(), f"batch {i} (M={sizes[i]})"
