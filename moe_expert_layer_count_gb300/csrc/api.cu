@@ -161,7 +161,7 @@ int scatter_impl(const void* hidden_states, int64_t M, int K, const TId* topk_id
                           local_num_experts, count_here ? nullptr : expert_num_tokens,
                           count_here ? expert_num_tokens : nullptr, count_here ? err_count : nullptr,
                           apply_router_weight_on_input ? 1 : 0, quant, a_out, a_scale, expert_offsets, src2dst,
-                          rp_cap, static_cast<int32_t*>(workspace), (cudaStream_t)stream);
+                          rp_cap, static_cast<int32_t*>(workspace), 0, (cudaStream_t)stream);
 }
 
 }  // namespace
@@ -319,7 +319,7 @@ int forward_chunked_impl(const void* hidden_states, const TId* topk_ids, const f
         const float* tw = topk_weights + c0 * topk;
         // the chunk's expert counts come out of the scatter's own histogram pass
         int st = launch_scatter(x + c0 * K, Mc, K, ids, tw, topk, expert_map, E, El, nullptr, counts, err_count,
-                                apply_router_weight_on_input ? 1 : 0, MOE_QUANT_FP8_1X128, A, sa, offs, s2d, cap, hist, s);
+                                apply_router_weight_on_input ? 1 : 0, MOE_QUANT_FP8_1X128, A, sa, offs, s2d, cap, hist, c0 > 0 ? 1 : 0, s);
         if (!st)
             st = launch_grouped_gemm(A, sa, w13, w13_scale, offs, counts, El, cap, 2 * N, K, MOE_EPI_SILU_MUL_QUANT, H, sh,
                                      sms, s);

@@ -77,7 +77,7 @@ int scatter_noalloc_impl(const void* hidden_states, int64_t M, int K, const TId*
     return launch_scatter(static_cast<const uint16_t*>(hidden_states), M, K, topk_ids, topk_weights, topk, expert_map,
                           E, local_num_experts, expert_num_tokens, nullptr, nullptr,
                           apply_router_weight_on_input ? 1 : 0, quant, a_out, a_scale, expert_offsets, src2dst, rp_cap,
-                          scratch, (cudaStream_t)stream);
+                          scratch, 0, (cudaStream_t)stream);
 }
 
 }  // namespace

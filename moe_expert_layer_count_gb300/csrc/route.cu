@@ -348,33 +348,16 @@ __global__ void __launch_bounds__(kScatterThreads)
     }
 }
 
-// One warp per (token, 512-column span): lane j holds 16 consecutive values, 8 lanes
-// form one 1x128 group. The row is read once and written to each of its kept slots.
+// One (token, 512-column span) unit of the row copy: lane j holds 16 consecutive values of
+// the span (raw0, raw1: its bf16 bits), 8 lanes form one 1x128 group; my_dst / my_w are
+// the token's slot destinations and weights, lane k holding slot k. The row was read
+// once and is written to each kept slot.
 template <bool kQuant>
-__global__ void __launch_bounds__(256)
-    scatter_copy_kernel(const uint16_t* __restrict__ x, int64_t M, int K, const int32_t* __restrict__ src2dst,
-                        const float* __restrict__ topk_weights, int topk, int apply_on_input,
-                        void* __restrict__ a_out, float* __restrict__ a_scale) {
-    const int lane = threadIdx.x & 31;
-    pdl_wait();
-    pdl_trigger();
-    const int spans = (K + 511) / 512;
-    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (gw >= M * spans) return;
-    const int64_t t = gw / spans;
-    const int g = (int)(gw % spans) * 4 + (lane >> 3);
+__device__ __forceinline__ void copy_unit(int lane, int K, int g, int col, bool active, int topk, int apply_on_input,
+                                          int my_dst, float my_w, uint4 raw0, uint4 raw1, void* __restrict__ a_out,
+                                          float* __restrict__ a_scale) {
     const int G = K / kGroup;
-    const bool active = g < G;
-    const int col = g * kGroup + (lane & 7) * 16;
-    const int my_dst = lane < topk ? __ldg(src2dst + t * topk + lane) : -1;
-    const float my_w = (lane < topk && apply_on_input) ? __ldg(topk_weights + t * topk + lane) : 1.f;
     float v[16];
-    uint4 raw0 = make_uint4(0, 0, 0, 0), raw1 = raw0;
-    if (active) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + t * K + col);
-        raw0 = __ldg(src);
-        raw1 = __ldg(src + 1);
-    }
     {
         const uint32_t w[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
 #pragma unroll
@@ -427,13 +410,211 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// One warp per (token, 512-column span).
+template <bool kQuant>
+__global__ void __launch_bounds__(256)
+    scatter_copy_kernel(const uint16_t* __restrict__ x, int64_t M, int K, const int32_t* __restrict__ src2dst,
+                        const float* __restrict__ topk_weights, int topk, int apply_on_input,
+                        void* __restrict__ a_out, float* __restrict__ a_scale) {
+    const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
+    const int spans = (K + 511) / 512;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= M * spans) return;
+    const int64_t t = gw / spans;
+    const int g = (int)(gw % spans) * 4 + (lane >> 3);
+    const bool active = g < K / kGroup;
+    const int col = g * kGroup + (lane & 7) * 16;
+    const int my_dst = lane < topk ? __ldg(src2dst + t * topk + lane) : -1;
+    const float my_w = (lane < topk && apply_on_input) ? __ldg(topk_weights + t * topk + lane) : 1.f;
+    uint4 raw0 = make_uint4(0, 0, 0, 0), raw1 = raw0;
+    if (active) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + t * K + col);
+        raw0 = __ldg(src);
+        raw1 = __ldg(src + 1);
+    }
+    copy_unit<kQuant>(lane, K, g, col, active, topk, apply_on_input, my_dst, my_w, raw0, raw1, a_out, a_scale);
+}
+
+// ------------------------------------------------------- scatter, small batches
+// For at most kSmallSlots top-k slots the whole scatter is one kernel: every CTA ranks all
+// the slots itself in shared memory (the same stable counting sort as the rank kernel: 8
+// contiguous warp segments, per-warp counts, expert offsets, per-warp cursors, ranks by
+// __match_any_sync), then copies and quantises its own (token, span) units. Ranking a few
+// thousand slots costs each CTA far less than the launch and the global round trip of a
+// separate index kernel. CTA 0 writes the offsets, counts and src2dst.
+// early != 0 (only for chunks after the first inside the chunk loop, where the kernel
+// still running before this one is the previous chunk's gather, which touches none of
+// these inputs): the ids, expert map, weights and the unit's row are read and ranked
+// before waiting for that kernel; every write still comes after the wait.
+constexpr int kSmallSlots = 4096;
+constexpr int kSmallGroups = kSmallSlots / (kScatterThreads / 32) / 32;  // groups of 32 per warp at most
+
+template <typename TId, bool kQuant>
+__global__ void __launch_bounds__(kScatterThreads)
+    scatter_small_kernel(const uint16_t* __restrict__ x, int64_t M, int K, const TId* __restrict__ ids,
+                         const float* __restrict__ topk_weights, int topk, const int32_t* __restrict__ expert_map,
+                         int E, int El, const int32_t* __restrict__ counts_in, int32_t* __restrict__ counts_out,
+                         int32_t* __restrict__ err_count, int apply_on_input, void* __restrict__ a_out,
+                         float* __restrict__ a_scale, int32_t* __restrict__ expert_offsets,
+                         int32_t* __restrict__ src2dst, int row_cap, int early) {
+    constexpr int kWarps = kScatterThreads / 32;
+    extern __shared__ int32_t sm[];
+    int32_t* off = sm;               // [El + 1]
+    int32_t* wc = off + El + 1;      // [kWarps][El]: per-warp counts, then per-warp cursors
+    int32_t* s_dst = wc + kWarps * El;  // [n]: permuted row of every slot, -1 if dropped
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n = (int)(M * topk);
+    if (!early) pdl_wait();
+    // this warp's copy unit: its row span is loaded first, so that the loads are in flight
+    // while the slots are ranked
+    const int spans = (K + 511) / 512;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+    const bool unit = gw < M * spans;
+    const int64_t t = unit ? gw / spans : 0;
+    const int g = (int)(gw % spans) * 4 + (lane >> 3);
+    const bool active = unit && g < K / kGroup;
+    const int col = g * kGroup + (lane & 7) * 16;
+    uint4 raw0 = make_uint4(0, 0, 0, 0), raw1 = raw0;
+    if (active) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + t * K + col);
+        raw0 = __ldg(src);
+        raw1 = __ldg(src + 1);
+    }
+    const float my_w = (unit && lane < topk && apply_on_input) ? __ldg(topk_weights + t * topk + lane) : 1.f;
+    // the warp's segment of the slots, in groups of 32
+    const int pw = ((n + kWarps - 1) / kWarps + 31) / 32 * 32;
+    const int wbeg = warp * pw, wend = min(n, wbeg + pw);
+    int lv[kSmallGroups];
+    int bad = 0;
+#pragma unroll
+    for (int j = 0; j < kSmallGroups; ++j) {
+        const int i = wbeg + j * 32 + lane;
+        lv[j] = (i < wend) ? local_expert(__ldg(ids + i), expert_map, E, El, bad) : -1;
+    }
+    for (int i = threadIdx.x; i < kWarps * El; i += kScatterThreads) wc[i] = 0;
+    __syncthreads();
+    int32_t* mine = wc + warp * El;
+#pragma unroll
+    for (int j = 0; j < kSmallGroups; ++j) {
+        if (wbeg + j * 32 >= wend) break;  // warp-uniform
+        const unsigned m = __match_any_sync(0xffffffffu, lv[j]);
+        if (lv[j] >= 0 && lane == __ffs(m) - 1) mine[lv[j]] += __popc(m);
+        __syncwarp();
+    }
+    __syncthreads();
+    const bool derive = counts_in == nullptr;
+    for (int l = threadIdx.x; l < El; l += kScatterThreads) {
+        int c = 0;
+        if (derive) {
+            for (int w = 0; w < kWarps; ++w) c += wc[w * El + l];
+        } else {
+            c = __ldg(counts_in + l);
+        }
+        off[l] = (c + kGroup - 1) / kGroup * kGroup;
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive scan of the padded block sizes, clamped to the row bound
+        int run = 0;
+        for (int lb = 0; lb < El; lb += 32) {
+            const int l = lb + lane;
+            const int c = l < El ? off[l] : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int tt = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += tt;
+            }
+            if (l < El) off[l] = min(run + incl - c, row_cap);
+            run = min(run + __shfl_sync(0xffffffffu, incl, 31), row_cap);
+        }
+        if (lane == 0) off[El] = run;
+    }
+    __syncthreads();
+    // per-warp cursors; the counts derived here are read back before they are overwritten
+    int cnt_l[4];  // at most El / kScatterThreads + 1 = 4 experts per thread for El <= 1024
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int l = threadIdx.x + q * kScatterThreads;
+        cnt_l[q] = 0;
+        if (l < El) {
+            int run = off[l];
+            for (int w = 0; w < kWarps; ++w) {
+                const int c = wc[w * El + l];
+                cnt_l[q] += c;
+                wc[w * El + l] = run;
+                run += c;
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kSmallGroups; ++j) {
+        if (wbeg + j * 32 >= wend) break;  // warp-uniform
+        const unsigned m = __match_any_sync(0xffffffffu, lv[j]);
+        const int rank = __popc(m & lanemask_lt());
+        int dst = -1;
+        if (lv[j] >= 0) {
+            dst = mine[lv[j]] + rank;
+            // counts given by the caller that disagree with the ids: the slot is dropped
+            if (dst >= off[lv[j] + 1]) dst = -1;
+        }
+        __syncwarp();
+        if (lv[j] >= 0 && rank == 0) mine[lv[j]] += __popc(m);
+        __syncwarp();
+        const int i = wbeg + j * 32 + lane;
+        if (i < wend) s_dst[i] = dst;
+    }
+    __syncthreads();
+    if (early) pdl_wait();
+    pdl_trigger();
+    if (blockIdx.x == 0) {
+        for (int l = threadIdx.x; l <= El; l += kScatterThreads) expert_offsets[l] = off[l];
+        if (derive) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int l = threadIdx.x + q * kScatterThreads;
+                if (l < El) counts_out[l] = cnt_l[q];
+            }
+            if (err_count) {
+#pragma unroll
+                for (int o = 16; o; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+                if (lane == 0 && bad) atomicAdd(err_count, bad);
+            }
+        }
+        for (int i = threadIdx.x; i < n; i += kScatterThreads) src2dst[i] = s_dst[i];
+    }
+    if (!unit) return;
+    const int my_dst = lane < topk ? s_dst[t * topk + lane] : -1;
+    copy_unit<kQuant>(lane, K, g, col, active, topk, apply_on_input, my_dst, my_w, raw0, raw1, a_out, a_scale);
+}
+
 template <typename TId>
 int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const float* topk_weights, int topk,
                    const int32_t* expert_map, int E, int El, const int32_t* counts_in, int32_t* counts_out,
                    int32_t* err_count, int apply_on_input, int quant, void* a_out, float* a_scale,
-                   int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, int32_t* hist, cudaStream_t stream) {
+                   int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, int32_t* hist, int early,
+                   cudaStream_t stream) {
     const int64_t n = M * topk;
     const int row_cap = (int)(rp_cap / kGroup * kGroup);
+    const size_t small_smem = (size_t)(El + 1 + (kScatterThreads / 32) * El + n) * sizeof(int32_t);
+    if (n <= kSmallSlots && small_smem <= 48 * 1024) {
+        const int64_t units = M * ((K + 511) / 512);
+        const unsigned sgrid = (unsigned)(units > 0 ? (units + 7) / 8 : 1);
+        const size_t smem = small_smem;
+        const int e = (early && !counts_in) ? 1 : 0;  // caller-given counts may come from the kernel before
+        if (quant == MOE_QUANT_FP8_1X128)
+            launch_k(scatter_small_kernel<TId, true>, sgrid, kScatterThreads, smem, stream, x, M, K, ids, topk_weights,
+                     topk, expert_map, E, El, counts_in, counts_out, err_count, apply_on_input, a_out, a_scale,
+                     expert_offsets, src2dst, row_cap, e);
+        else
+            launch_k(scatter_small_kernel<TId, false>, sgrid, kScatterThreads, smem, stream, x, M, K, ids, topk_weights,
+                     topk, expert_map, E, El, counts_in, counts_out, err_count, apply_on_input, a_out, a_scale,
+                     expert_offsets, src2dst, row_cap, e);
+        note_launches(1);
+        return launch_status();
+    }
     const int per_cta = scatter_slots_per_cta(n);
     const int grid = (int)((n + per_cta - 1) / per_cta);
     const size_t smem_rank = (size_t)(3 * El + 1 + (kScatterThreads / 32) * El) * sizeof(int32_t);
@@ -459,7 +640,7 @@ int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const fl
 #define MOE_INSTANTIATE_SCATTER(TId)                                                                              \
     template int launch_scatter<TId>(const uint16_t*, int64_t, int, const TId*, const float*, int, const int32_t*, \
                                      int, int, const int32_t*, int32_t*, int32_t*, int, int, void*, float*,         \
-                                     int32_t*, int32_t*, int64_t, int32_t*, cudaStream_t);
+                                     int32_t*, int32_t*, int64_t, int32_t*, int, cudaStream_t);
 MOE_INSTANTIATE_SCATTER(int32_t)
 MOE_INSTANTIATE_SCATTER(int64_t)
 #undef MOE_INSTANTIATE_SCATTER

@@ -21,11 +21,15 @@ int launch_count(const TId* ids, int64_t n, const int32_t* expert_map, int E, in
 // counts_in NULL: the experts' slot counts are derived by the scatter's own histogram
 // pass and written to counts_out (bad ids then added to err_count, if not NULL).
 // rp_cap: rows of a_out / a_scale; expert_offsets never exceed it (rounded down to 128).
+// early != 0: the only kernel that can still be running before this call's first kernel
+// is this library's gather of an earlier chunk, so inputs may be read before waiting for
+// it (small batches only; every write still waits).
 template <typename TId>
 int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const float* topk_weights, int topk,
                    const int32_t* expert_map, int E, int El, const int32_t* counts_in, int32_t* counts_out,
                    int32_t* err_count, int apply_on_input, int quant, void* a_out, float* a_scale,
-                   int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, int32_t* hist, cudaStream_t stream);
+                   int32_t* expert_offsets, int32_t* src2dst, int64_t rp_cap, int32_t* hist, int early,
+                   cudaStream_t stream);
 
 int launch_gather(const uint16_t* y, const int32_t* src2dst, const float* topk_weights, int64_t M, int topk, int K,
                   int apply_on_input, uint16_t* out, cudaStream_t stream);
