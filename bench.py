@@ -246,9 +246,7 @@ def run_count_only(args, world, local_rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic: seeded N(0,1) router logits, top-8 of 128 experts",
-        "config": {"workload": wl.name, "M": wl.M, "experts": wl.E, "topk": wl.topk, "step": "count only",
-                   "l2": "flushed before every timed step (256 MB write); each step timed by its own events",
-                   "parallelism": f"replicas x{world} (one independent batch per GPU)"},
+        "config": workload_config(wl, world),
         "gpu_launches": int(launches), "clocks": clk.summary(),
         "roofline": {"kernel": "count", "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
                      "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
@@ -402,17 +400,11 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "fp8_e4m3" if not permute_only else "bf16/fp8_e4m3",
         "data": "synthetic: seeded N(0,1) bf16 tokens, N(0,1)+Zipf router logits, random-init N(0,0.02) "
                 "weights quantised to FP8 e4m3 with 128x128 block scales",
-        "config": {"workload": wl.name, "M": M, "hidden": K, "moe_intermediate": N, "experts": E,
-                   "local_experts": El, "topk": topk, "chunk_size": chunk,
-                   "routing": f"zipf s={wl.zipf_s}" if wl.zipf_s else "uniform",
-                   "cuda_graph": bool(args.graph),
-                   "routing_batches": f"{R} (router seeds {wl.seed}..{wl.seed + R - 1}, step i runs batch i % {R}; "
-                                      f"per-kernel breakdown and roofline on batch 0)",
-                   "parallelism": f"replicas x{world} (one independent batch per GPU)",
-                   "l2": "inputs larger than L2 (expert weights %.0f MB + activations)" %
-                         (work.get("weight_bytes", 0) / 1e6) if not permute_only else
-                         "inputs larger than L2 (x %.0f MB + permuted rows %.0f MB)" %
-                         (M * K * 2 / 1e6, work["R"] * K * 3 / 1e6)},
+        "config": workload_config(wl, world),
+        "run": {"cuda_graph": bool(args.graph),
+                "routing_batches": f"{R} (router seeds {wl.seed}..{wl.seed + R - 1}, step i runs batch i % {R}; "
+                                   f"per-kernel breakdown and roofline on batch 0)",
+                "touched_weight_mb": round(work.get("weight_bytes", 0) / 1e6, 1)},
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
         "roofline": roof,
@@ -604,66 +596,120 @@ def end_to_end(moe, torch, stream, li, dev, args, step_dev, x, routes, out, laye
             "api": "moe_forward_host (pipelined)" if layer is not None else "moe_scatter + moe_gather_weight_reduce"}
 
 
+# ------------------------------------------------------------------ config
+def workload_config(wl, world):
+    """The JSON line's `config`: the workload, its shape and the L2 rule, the same for
+    both arms."""
+    c = {"workload": wl.name, "M": wl.M, "hidden": wl.K}
+    if wl.N:
+        c["moe_intermediate"] = wl.N
+    c.update({"experts": wl.E, "local_experts": wl.El, "topk": wl.topk, "chunk_size": wl.chunk,
+              "routing": f"zipf s={wl.zipf_s}" if wl.zipf_s else "uniform",
+              "parallelism": f"replicas x{world} (one independent batch per GPU)"})
+    if wl.name == mi.COUNT_ONLY.name:
+        c["step"] = "count only"
+        c["l2"] = "flushed before every timed step (256 MB write); each step timed by its own events"
+    elif wl.N:
+        c["l2"] = "inputs larger than L2: the touched experts' FP8 weights alone exceed the 129 MB L2"
+    else:
+        c["l2"] = "inputs larger than L2: hidden states + permuted rows + unpermuted output exceed it"
+    return c
+
+
 # ------------------------------------------------------------------- CPU oracle
-def oracle_sample(wl, target_s=12.0):
-    """Times the CPU oracle (as it stands, single-threaded C) on a bounded sample of the
-    workload: its first m tokens, m grown until one call takes ~target_s."""
-    import oracle
+ORACLE_BUDGET_S = 90.0  # wall time the reference arm's timed + warm-up oracle calls may take
+
+
+def _oracle_inputs(wl):
     count_only = wl.name == mi.COUNT_ONLY.name
     if count_only:  # only the routing is needed
         ids, w = mi.route(wl.M, wl.E, wl.topk, wl.seed, wl.zipf_s)
-        li = mi.LayerInputs(wl, np.zeros((wl.M, 0), np.uint16), ids, w, None)
+        return mi.LayerInputs(wl, np.zeros((wl.M, 0), np.uint16), ids, w, None)
+    return mi.make_layer_inputs(wl)
+
+
+def _oracle_call(wl, li, m, parallel):
+    """One oracle pass over the first m tokens of the workload (the OpenMP build when
+    parallel; only the layer has a multi-threaded row loop)."""
+    import oracle
+    if wl.name == mi.COUNT_ONLY.name:
+        oracle.count(li.topk_ids[:m], wl.E, wl.El)
+    elif wl.N:
+        oracle.forward_chunked(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], li.w13, li.w13_scale, li.w2,
+                               li.w2_scale, wl.E, expert_map=li.expert_map, chunk_size=wl.chunk, parallel=parallel)
     else:
-        li = mi.make_layer_inputs(wl)
-    m = 4
-    while True:
+        r = oracle.scatter(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], wl.E, wl.El, li.expert_map)
+        oracle.gather(mi.bf16_bits(np.zeros((r["a"].shape[0], wl.K), np.float32)), r["src2dst"],
+                      li.topk_weights[:m])
+
+
+def oracle_sample(wl, calls, budget_s=ORACLE_BUDGET_S):
+    """The token sample both CPU legs time: the first m tokens, m the largest power of two
+    (at most M) whose OpenMP oracle pass, repeated `calls` times, fits in budget_s
+    (estimated from a calibration pass). Returns (inputs, m)."""
+    li = _oracle_inputs(wl)
+    m0 = min(wl.M, 8 if wl.N else 1024)
+    t0 = time.perf_counter()
+    _oracle_call(wl, li, m0, True)
+    per_token = max(1e-9, (time.perf_counter() - t0) / m0)
+    fit = budget_s / max(1, calls) / per_token
+    m = 1
+    while m * 2 <= min(wl.M, fit):
+        m *= 2
+    return li, max(1, min(m, wl.M))
+
+
+def _timed(wl, li, m, parallel, min_s):
+    """Tokens/s of repeated oracle passes over m tokens, at least one pass and min_s."""
+    n, t = 0, 0.0
+    while n == 0 or t < min_s:
         t0 = time.perf_counter()
-        if count_only:
-            oracle.count(li.topk_ids[:m], wl.E, wl.El)
-        elif wl.N:
-            oracle.forward_chunked(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], li.w13, li.w13_scale, li.w2,
-                                   li.w2_scale, wl.E, expert_map=li.expert_map, chunk_size=wl.chunk)
-        else:
-            r = oracle.scatter(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], wl.E, wl.El, li.expert_map)
-            oracle.gather(mi.bf16_bits(np.zeros((r["a"].shape[0], wl.K), np.float32)), r["src2dst"],
-                          li.topk_weights[:m])
-        dt = time.perf_counter() - t0
-        if dt >= target_s or m >= wl.M:
-            return li, m, dt
-        m = min(wl.M, max(m * 2, int(m * target_s / max(dt, 1e-3) * 1.1)))
+        _oracle_call(wl, li, m, parallel)
+        t += time.perf_counter() - t0
+        n += 1
+    return m * n / t, n, t
 
 
-def cpu_baseline(wl):
-    _, m, dt = oracle_sample(wl)
-    return {"value": round(m / dt, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {m} of {wl.M} tokens of {wl.name} (single-threaded C oracle, {dt:.1f} s)"}
+def cpu_baseline(wl, calls):
+    """The oracle as it stands on the host cores: its OpenMP build over all cores (the
+    reported value) and the single-threaded checker, on the reference arm's sample."""
+    import oracle
+    li, m = oracle_sample(wl, calls)
+    par = bool(wl.N) and wl.name != mi.COUNT_ONLY.name
+    v, n, t = _timed(wl, li, m, par, 8.0)
+    v1, n1, t1 = _timed(wl, li, m, False, 8.0)
+    cores = oracle.num_threads(True) if par else 1
+    return {"value": round(v, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {m} of {wl.M} tokens of {wl.name}, {n} passes in {t:.1f} s "
+                      f"({'OpenMP C oracle' if par else 'single-threaded C oracle'})",
+            "single_thread": {"value": round(v1, 3), "unit": "tokens/s", "cores": 1,
+                              "sample": f"first {m} tokens, {n1} passes in {t1:.1f} s"}}
 
 
 def run_reference(args):
-    wl = mi.WORKLOADS[args.workload]
-    li, m, _ = oracle_sample(wl, target_s=4.0)
+    """The reference arm: the CPU oracle (OpenMP build, all host cores) on the same token
+    sample the CPU-baseline leg times, W warm-up and K timed passes."""
     import oracle
+    wl = mi.WORKLOADS[args.workload]
+    li, m = oracle_sample(wl, args.warmup + args.steps)
+    par = bool(wl.N) and wl.name != mi.COUNT_ONLY.name
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        if wl.name == mi.COUNT_ONLY.name:
-            oracle.count(li.topk_ids[:m], wl.E, wl.El)
-        elif wl.N:
-            oracle.forward_chunked(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], li.w13, li.w13_scale, li.w2,
-                                   li.w2_scale, wl.E, expert_map=li.expert_map, chunk_size=wl.chunk)
-        else:
-            r = oracle.scatter(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], wl.E, wl.El, li.expert_map)
+        _oracle_call(wl, li, m, par)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     s = sum(times)
     value = m * len(times) / s
+    cores = oracle.num_threads(True) if par else 1
     return {"impl": "reference", "metric": "MoE-layer tokens/s", "value": round(value, 3), "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(s / len(times) * 1e3, 2), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp64 (oracle)", "data": "synthetic",
-            "config": {"workload": wl.name, "M": wl.M, "sample_tokens_per_step": m},
-            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"first {m} of {wl.M} tokens per step"},
+            "config": workload_config(wl, args.gpus),
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {m} of {wl.M} tokens per pass "
+                                       f"({'OpenMP C oracle' if par else 'single-threaded C oracle'})"},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -688,7 +734,7 @@ def main():
         line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(mi.WORKLOADS[args.workload])
+            line["cpu_baseline"] = cpu_baseline(mi.WORKLOADS[args.workload], args.warmup + args.steps)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

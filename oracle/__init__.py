@@ -25,16 +25,22 @@ from . import build as _build
 _HERE = os.path.dirname(os.path.abspath(__file__))
 GROUP = 128
 
-_lib = None
+_libs = {}
 
 
-def lib() -> ctypes.CDLL:
-    global _lib
-    if _lib is None:
-        path = _build.build()
-        _lib = ctypes.CDLL(path)
-        _declare(_lib)
-    return _lib
+def lib(parallel: bool = False) -> ctypes.CDLL:
+    """The single-threaded oracle (the checker), or with parallel=True its OpenMP build
+    (the timed CPU baseline; identical results)."""
+    if parallel not in _libs:
+        L = ctypes.CDLL(_build.build(parallel=parallel))
+        _declare(L)
+        _libs[parallel] = L
+    return _libs[parallel]
+
+
+def num_threads(parallel: bool = True) -> int:
+    """Host threads the oracle's row loop runs on."""
+    return int(lib(parallel).oracle_num_threads())
 
 
 _p = ctypes.c_void_p
@@ -70,6 +76,8 @@ def _declare(L):
     L.oracle_forward_token.argtypes = [_i64, _p, _p, _p, _p, _p, _p, _p, _p, _int, _int,
                                        _int, _int, _int, _int, _p]
     L.oracle_forward_token.restype = None
+    L.oracle_num_threads.argtypes = []
+    L.oracle_num_threads.restype = _int
 
 
 def _c(a: np.ndarray, dtype) -> np.ndarray:
@@ -199,8 +207,9 @@ def gather(Y_bits, src2dst, topk_weights, apply_router_weight_on_input=False):
 
 
 def forward_chunked(x_bits, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, E,
-                    expert_map=None, chunk_size=None, apply_router_weight_on_input=False):
-    """Step a7: the whole layer under the chunking loop, bf16 bits [M, K]."""
+                    expert_map=None, chunk_size=None, apply_router_weight_on_input=False, parallel=False):
+    """Step a7: the whole layer under the chunking loop, bf16 bits [M, K] (parallel=True:
+    the OpenMP build, same result)."""
     x = _c(x_bits, np.uint16)
     ids = _ids(topk_ids)
     w = _c(topk_weights, np.float32)
@@ -214,7 +223,7 @@ def forward_chunked(x_bits, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale
     topk = ids.shape[1]
     chunk = M if chunk_size is None else int(chunk_size)
     out = np.zeros((M, K), np.uint16)
-    bad = lib().oracle_forward_chunked(_ptr(x), _ptr(ids), _ptr(w), _ptr(w13), _ptr(s13),
+    bad = lib(parallel).oracle_forward_chunked(_ptr(x), _ptr(ids), _ptr(w), _ptr(w13), _ptr(s13),
                                        _ptr(w2), _ptr(s2), _ptr(m), E, El, M, K, N2 // 2, topk,
                                        max(chunk, 1), int(bool(apply_router_weight_on_input)),
                                        _ptr(out))

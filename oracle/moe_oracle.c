@@ -20,7 +20,16 @@
  * for the GEMM dot products (the per-128 partial sums of fp8 x fp8 products are exact
  * in fp64), bf16 round-to-nearest-even where the layer stores bf16.
  * Build with -ffp-contract=off so that no multiply-add is fused.
+ *
+ * Built twice: single-threaded (the checker the tests use) and with -fopenmp (the CPU
+ * baseline timed over all host cores). The OpenMP build only spreads the independent
+ * permuted rows of the chunking loop over threads, each with its own scratch; every
+ * row's arithmetic is the same code in the same order, so both builds give identical
+ * results.
  */
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -316,27 +325,46 @@ int64_t oracle_forward_chunked(const uint16_t* x, const int64_t* topk_ids, const
     int32_t* offsets = (int32_t*)malloc((size_t)(El + 1) * sizeof(int32_t));
     int32_t* counts = (int32_t*)malloc((size_t)El * sizeof(int32_t));
     int32_t* src2dst = (int32_t*)malloc((size_t)cmax * topk * sizeof(int32_t));
-    float* c1 = (float*)malloc((size_t)2 * N * sizeof(float));
-    float* h = (float*)malloc((size_t)N * sizeof(float));
-    uint8_t* hq = (uint8_t*)malloc((size_t)N);
-    float* hs = (float*)malloc((size_t)(N / GROUP) * sizeof(float));
+    int64_t* kept_row = (int64_t*)malloc((size_t)cmax * topk * sizeof(int64_t));
+    int* kept_expert = (int*)malloc((size_t)cmax * topk * sizeof(int));
     for (int64_t c0 = 0; c0 < M; c0 += chunk_size) {
         int64_t Mc = (M - c0) < chunk_size ? (M - c0) : chunk_size;
         bad += oracle_scatter(x + c0 * K, Mc, K, topk_ids + c0 * topk, topk_weights + c0 * topk, topk,
                               expert_map, E, El, apply_router_weight_on_input, 1, A, sa, offsets, src2dst);
         oracle_count(topk_ids + c0 * topk, Mc, topk, expert_map, E, El, counts);
+        /* the kept rows; rows [offsets[l] + counts[l], offsets[l + 1]) are padding and never read */
+        int64_t nk = 0;
         for (int l = 0; l < El; ++l)
-            /* rows [offsets[l] + counts[l], offsets[l + 1]) are padding and never read */
-            for (int64_t r = offsets[l]; r < (int64_t)offsets[l] + counts[l]; ++r)
-                expert_row(A + r * K, sa + r * (K / GROUP), l, w13, w13_scale, w2, w2_scale, K, N, c1, h, hq,
-                           hs, Y + r * K);
+            for (int64_t r = offsets[l]; r < (int64_t)offsets[l] + counts[l]; ++r) {
+                kept_row[nk] = r;
+                kept_expert[nk++] = l;
+            }
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+        {
+            float* c1 = (float*)malloc((size_t)2 * N * sizeof(float));
+            float* h = (float*)malloc((size_t)N * sizeof(float));
+            uint8_t* hq = (uint8_t*)malloc((size_t)N);
+            float* hs = (float*)malloc((size_t)(N / GROUP) * sizeof(float));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t i = 0; i < nk; ++i) {
+                const int64_t r = kept_row[i];
+                expert_row(A + r * K, sa + r * (K / GROUP), kept_expert[i], w13, w13_scale, w2, w2_scale, K, N, c1,
+                           h, hq, hs, Y + r * K);
+            }
+            free(hs);
+            free(hq);
+            free(h);
+            free(c1);
+        }
         oracle_gather(Y, src2dst, topk_weights + c0 * topk, Mc, topk, K, apply_router_weight_on_input,
                       out + c0 * K);
     }
-    free(hs);
-    free(hq);
-    free(h);
-    free(c1);
+    free(kept_expert);
+    free(kept_row);
     free(src2dst);
     free(counts);
     free(offsets);
@@ -389,4 +417,13 @@ void oracle_forward_token(int64_t t, const uint16_t* x, const int64_t* topk_ids,
     free(sa);
     free(a);
     free(row);
+}
+
+/* Threads the OpenMP build runs the row loop on (1 in the single-threaded build). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
 }

@@ -452,3 +452,17 @@ def test_layer_single_expert_matches_numpy_pipeline():
     err = np.abs(got - ref)
     assert err.max() <= 2e-2 * np.abs(ref).max()
     assert err.sum() / np.abs(ref).sum() <= 5e-3
+
+
+def test_openmp_build_equals_single_threaded():
+    """The OpenMP build (the timed CPU baseline) only spreads independent rows over
+    threads: its layer output is bit-identical to the single-threaded checker's."""
+    li = mi.make_layer_inputs(mi.TINY)
+    wl = li.wl
+    args = (li.x, li.topk_ids, li.topk_weights, li.w13, li.w13_scale, li.w2, li.w2_scale, wl.E)
+    for chunk in (None, 7):
+        single = oracle.forward_chunked(*args, chunk_size=chunk)
+        par = oracle.forward_chunked(*args, chunk_size=chunk, parallel=True)
+        assert (single == par).all()
+    assert oracle.num_threads(parallel=False) == 1
+    assert oracle.num_threads(parallel=True) >= 1
