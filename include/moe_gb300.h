@@ -276,6 +276,23 @@ MOE_API int moe_forward_chunked_i64(const void* hidden_states, const int64_t* to
                                     int apply_router_weight_on_input, void* out, void* workspace,
                                     size_t workspace_bytes, int32_t* err_count, moe_stream_t stream);
 
+/* Expert-parallel combine (vLLM PR #20903 "[Kernel] DeepGemm MoE : Integrate triton
+ * permute / unpermute kernels", Purpose: DeepEP high-throughput prepare/finalize with
+ * expert parallelism). A rank that holds a subset of the experts runs the layer with an
+ * expert_map and gets its share of every token's sum over its top-k experts (a zero row
+ * for tokens whose experts are all elsewhere); the layer output is the sum of the shares.
+ * After the caller has gathered the shares of all ranks on this GPU (an all-gather; the
+ * exchange is not part of this library), this call adds them:
+ *   out[t, c] = bf16( sum over r = 0..n_parts-1, in ascending r, of partials[r][t, c] ),
+ * accumulated in fp32 with separately rounded adds.
+ *   partials  HOST array of n_parts (1..64) DEVICE pointers, each bf16 [M, K], 16-byte aligned
+ *   out       bf16 [M, K], 16-byte aligned, overlapping no part
+ *   K         a multiple of 8
+ * The sum of bf16 shares differs from a single-GPU run of the whole layer (one rounding
+ * of the full top-k sum) by the rounding of each share. */
+MOE_API int moe_ep_combine(const void* const* partials, int n_parts, int64_t M, int K, void* out,
+                           moe_stream_t stream);
+
 /* Workspace bytes moe_forward_host (or _i64) needs for batches of up to M tokens: the
  * layer's own workspace (moe_workspace_size for min(chunk_size, M)) followed by two
  * staging slots, each a device copy of a batch's hidden_states, topk_ids (room for int64

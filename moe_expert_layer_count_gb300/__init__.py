@@ -75,6 +75,7 @@ SIGNATURES = {
     "moe_forward_chunked_i64": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
                                  _p, _p, _sz, _p, _p], _int),
     "moe_host_workspace_size": ([_i64, _int, _int, _int, _int, _i64], _sz),
+    "moe_ep_combine": ([_p, _int, _i64, _int, _p, _p], _int),
     "moe_forward_host": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
                           _p, _p, _sz, _p, _p, _p], _int),
     "moe_forward_host_i64": ([_p, _p, _p, _p, _p, _p, _p, _p, _int, _int, _i64, _int, _int, _int, _i64, _int,
@@ -346,3 +347,20 @@ def moe_forward_host(hidden_states, topk_ids, topk_weights, w13, w13_scale, w2, 
 def moe_host_wait(stream=None):
     """Orders `stream` after every output copy moe_forward_host has enqueued so far."""
     _check("moe_host_wait", lib().moe_host_wait(_stream(stream)))
+
+
+def moe_ep_combine(partials, out=None, stream=None):
+    """Sum of the ranks' partial layer outputs (bf16 [M, K] CUDA tensors, in rank order):
+    fp32 accumulation in ascending rank order, one rounding to bf16."""
+    if not partials:
+        raise ValueError("moe_ep_combine: no partial outputs")
+    for p in partials:
+        _dt(p, torch.bfloat16, "partials")
+    M, K = partials[0].shape
+    if any(tuple(p.shape) != (M, K) for p in partials):
+        raise ValueError("moe_ep_combine: partial outputs of different shapes")
+    if out is None:
+        out = torch.empty(M, K, dtype=torch.bfloat16, device=partials[0].device)
+    arr = (ctypes.c_void_p * len(partials))(*[_ptr(p).value for p in partials])
+    _check("moe_ep_combine", lib().moe_ep_combine(arr, len(partials), M, K, _ptr(out), _stream(stream)))
+    return out

@@ -76,6 +76,8 @@ def _declare(L):
     L.oracle_forward_token.argtypes = [_i64, _p, _p, _p, _p, _p, _p, _p, _p, _int, _int,
                                        _int, _int, _int, _int, _p]
     L.oracle_forward_token.restype = None
+    L.oracle_ep_combine.argtypes = [_p, _int, _i64, _int, _p]
+    L.oracle_ep_combine.restype = None
     L.oracle_num_threads.argtypes = []
     L.oracle_num_threads.restype = _int
 
@@ -252,4 +254,15 @@ def forward_tokens(tokens, x_bits, topk_ids, topk_weights, w13, w13_scale, w2, w
         lib().oracle_forward_token(int(t), _ptr(x), _ptr(ids), _ptr(w), _ptr(w13), _ptr(s13),
                                    _ptr(w2), _ptr(s2), _ptr(m), E, El, K, N2 // 2, topk,
                                    int(bool(apply_router_weight_on_input)), _ptr(out[i]))
+    return out
+
+
+def ep_combine(parts):
+    """Expert-parallel combine: the sum of the ranks' partial outputs (bf16 bits [M, K]
+    each, in rank order), fp32 in ascending rank order, one rounding to bf16."""
+    ps = [_c(p, np.uint16) for p in parts]
+    M, K = ps[0].shape
+    arr = (ctypes.c_void_p * len(ps))(*[p.ctypes.data for p in ps])
+    out = np.zeros((M, K), np.uint16)
+    lib().oracle_ep_combine(arr, len(ps), M, K, _ptr(out))
     return out

@@ -427,3 +427,15 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Expert-parallel combine (P1 Purpose: DeepEP high-throughput prepare/finalize with
+ * expert parallelism; reading C10: a rank's layer output is its share of each token's
+ * top-k sum). The full output is the sum of the n_parts shares (bf16 [M, K] each):
+ * fp32 accumulation in ascending part order, one rounding to bf16. */
+void oracle_ep_combine(const uint16_t* const* parts, int n_parts, int64_t M, int K, uint16_t* out) {
+    for (int64_t i = 0; i < M * K; ++i) {
+        float acc = 0.0f;
+        for (int r = 0; r < n_parts; ++r) acc = acc + bf16_to_f32(parts[r][i]);
+        out[i] = f32_to_bf16(acc);
+    }
+}

@@ -466,3 +466,44 @@ def test_openmp_build_equals_single_threaded():
         assert (single == par).all()
     assert oracle.num_threads(parallel=False) == 1
     assert oracle.num_threads(parallel=True) >= 1
+
+
+def test_ep_combine_pins():
+    """Expert-parallel combine: one share is returned unchanged; shares of exactly
+    representable values add exactly; and the fp32 sum runs in ascending rank order:
+    2^24 + 1 + 1 - 2^24 is 0 that way (2^24 + 1 rounds to 2^24 in fp32, twice), while a
+    pairwise sum would give 2."""
+    rng = np.random.default_rng(0)
+    x = mi.bf16_bits(rng.standard_normal((5, 16)).astype(np.float32))
+    assert (oracle.ep_combine([x]) == x).all()
+    a = mi.bf16_bits(np.full((2, 8), 1.5, np.float32))
+    b = mi.bf16_bits(np.full((2, 8), -0.25, np.float32))
+    c = mi.bf16_bits(np.full((2, 8), 4.0, np.float32))
+    assert (mi.bf16_to_f32(oracle.ep_combine([a, b, c])) == 5.25).all()
+    big = mi.bf16_bits(np.full((1, 8), 2.0 ** 24, np.float32))
+    one = mi.bf16_bits(np.full((1, 8), 1.0, np.float32))
+    neg = mi.bf16_bits(np.full((1, 8), -(2.0 ** 24), np.float32))
+    assert (mi.bf16_to_f32(oracle.ep_combine([big, one, one, neg])) == 0.0).all()
+    assert (mi.bf16_to_f32(oracle.ep_combine([one, one, big, neg])) == 2.0).all()
+    # one rounding at the end: 1 + 2^-8 (not a bf16) arises only inside the sum
+    s = oracle.ep_combine([one, mi.bf16_bits(np.full((1, 8), 2.0 ** -8, np.float32))])
+    assert (mi.bf16_to_f32(s) == 1.0).all()  # 1 + 2^-8 is a tie in bf16: rounds to even (1.0)
+
+
+def test_ep_combine_of_expert_shares_is_the_layer(tiny):
+    """Shares from four expert subsets (2 experts each) sum to the single-GPU layer
+    output up to the bf16 rounding of each share."""
+    li = tiny
+    E = li.wl.E
+    full = mi.bf16_to_f32(oracle.forward_chunked(li.x, li.topk_ids, li.topk_weights, li.w13, li.w13_scale,
+                                                 li.w2, li.w2_scale, E))
+    parts = []
+    for lo in range(0, E, 2):
+        m = np.full(E, -1, np.int32)
+        m[lo:lo + 2] = np.arange(2)
+        sl = slice(lo, lo + 2)
+        parts.append(oracle.forward_chunked(li.x, li.topk_ids, li.topk_weights, li.w13[sl], li.w13_scale[sl],
+                                            li.w2[sl], li.w2_scale[sl], E, expert_map=m))
+    got = mi.bf16_to_f32(oracle.ep_combine(parts))
+    err = np.abs(got - full)
+    assert err.max() <= 2e-2 * np.abs(full).max() and err.sum() <= 5e-3 * np.abs(full).sum()
