@@ -27,7 +27,8 @@
 //    and one amax exchange per row (shared memory and a hardware named barrier over the
 //    8 epilogue warps) completes the 128-wide group.
 // Small batches (given the experts' valid row counts) run a variant in which an epilogue
-// warp whose 32 rows are all padding skips the TMEM reads, folding and stores.
+// warp whose 32 rows are all padding skips the TMEM reads, folding and stores, and in
+// which a tile whose kept rows all lie in its first 32 (or 64) loads only those rows of A.
 // Every wait on a pipeline barrier gives up after 2 s, sets a device error word and an
 // abort flag seen by all roles, waits (bounded) for its own copies and MMAs in flight,
 // and the CTA frees its TMEM and returns. An epilogue warp that gives up arrives on the
@@ -169,7 +170,8 @@ __device__ __forceinline__ int expert_of(const int32_t* s_off, int El, int row0)
 
 template <int BN, int EPI, bool kSkip>
 __global__ void __launch_bounds__(threads_of<EPI>(), 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
+                   const __grid_constant__ CUtensorMap tmA64, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, const float* __restrict__ sa, const float* __restrict__ sw,
                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts,
                    int El, int row_cap, int n_out, int k_in, void* __restrict__ out, float* __restrict__ out_scale) {
@@ -213,6 +215,10 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
     }
     if (warp == kProducerWarp && lane == 0) {
         ptx::prefetch_tmap(&tmA);
+        if (kSkip) {
+            ptx::prefetch_tmap(&tmA32);
+            ptx::prefetch_tmap(&tmA64);
+        }
         ptx::prefetch_tmap(&tmB);
         ptx::prefetch_tmap(&tmO);
     }
@@ -242,15 +248,26 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                 const int mt = tile / n_tiles, nt = tile % n_tiles;
                 const int row0 = mt * kBM;
                 const int l = expert_of(s_off, El, row0);
+                // small batches: when all of the tile's kept rows lie in its first 32 (64),
+                // only those rows of A are loaded (the rest of the tile's A stays whatever
+                // the stage held before: those rows are padding, whose warps neither fold
+                // nor store anything)
+                int a_rows = kBM;
+                if constexpr (kSkip) {
+                    const int kept = s_off[l] + s_cnt[l] - row0;
+                    a_rows = kept <= 32 ? 32 : kept <= 64 ? 64 : kBM;
+                }
+                const CUtensorMap* tma = a_rows == 32 ? &tmA32 : a_rows == 64 ? &tmA64 : &tmA;
+                const uint32_t stage_bytes = C::kStageBytes - (uint32_t)(kBM - a_rows) * kBK;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % C::kStages;
                     const uint32_t ph = (it / C::kStages) & 1;
                     if (!wait_phase(ptx::smem_addr(&st->empty[s]), ph ^ 1, abort)) { ok = false; break; }
                     const uint32_t full = ptx::smem_addr(&st->full[s]);
-                    ptx::mbar_arrive_expect_tx(full, C::kStageBytes);
+                    ptx::mbar_arrive_expect_tx(full, stage_bytes);
                     const uint32_t a_dst = ptx::smem_addr(smem + s * C::kStageBytes);
                     const uint32_t b_dst = a_dst + C::kABytes;
-                    ptx::tma_load_2d(a_dst, &tmA, kb * kBK, row0, full);
+                    ptx::tma_load_2d(a_dst, tma, kb * kBK, row0, full);
 #pragma unroll
                     for (int p = 0; p < BN / kBoxRows; ++p) {
                         int brow;
@@ -604,7 +621,8 @@ bool make_out_tmap(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, int
 }
 
 template <int BN, int EPI, bool kSkip>
-int launch_tc_k(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const float* a_scale,
+int launch_tc_k(const CUtensorMap& ta, const CUtensorMap& ta32, const CUtensorMap& ta64, const CUtensorMap& tb, const CUtensorMap& to,
+                const float* a_scale,
                 const float* w_scale, const int32_t* offsets, const int32_t* counts, int El, int64_t rp_cap,
                 int n_out, int k_in, void* out, float* out_scale, int num_sms, cudaStream_t stream) {
     const size_t smem = smem_bytes<BN, EPI>(El);
@@ -623,7 +641,7 @@ int launch_tc_k(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
     const int64_t max_tiles = rp_cap / kBM * n_tiles;
     const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid < 1) return MOE_OK;
-    launch_k(gemm_tc_kernel<BN, EPI, kSkip>, grid, threads_of<EPI>(), smem, stream, ta, tb, to, a_scale, w_scale,
+    launch_k(gemm_tc_kernel<BN, EPI, kSkip>, grid, threads_of<EPI>(), smem, stream, ta, ta32, ta64, tb, to, a_scale, w_scale,
              offsets, counts, El, (int)rp_cap, n_out, k_in, out, out_scale);
     note_launches(1);
     return launch_status();
@@ -633,13 +651,14 @@ int launch_tc_k(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
 // of each block is padding) run the kernel that skips all-padding row groups; large ones
 // the kernel without that path, which leaves its registers to the full tiles.
 template <int BN, int EPI>
-int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const float* a_scale,
+int launch_tc(const CUtensorMap& ta, const CUtensorMap& ta32, const CUtensorMap& ta64, const CUtensorMap& tb, const CUtensorMap& to,
+              const float* a_scale,
               const float* w_scale, const int32_t* offsets, const int32_t* counts, int El, int64_t rp_cap, int n_out,
               int k_in, void* out, float* out_scale, int num_sms, cudaStream_t stream) {
     if (counts && rp_cap < (int64_t)El * 2 * kBM)
-        return launch_tc_k<BN, EPI, true>(ta, tb, to, a_scale, w_scale, offsets, counts, El, rp_cap, n_out, k_in, out,
+        return launch_tc_k<BN, EPI, true>(ta, ta32, ta64, tb, to, a_scale, w_scale, offsets, counts, El, rp_cap, n_out, k_in, out,
                                           out_scale, num_sms, stream);
-    return launch_tc_k<BN, EPI, false>(ta, tb, to, a_scale, w_scale, offsets, counts, El, rp_cap, n_out, k_in, out,
+    return launch_tc_k<BN, EPI, false>(ta, ta32, ta64, tb, to, a_scale, w_scale, offsets, counts, El, rp_cap, n_out, k_in, out,
                                        out_scale, num_sms, stream);
 }
 
@@ -656,26 +675,28 @@ int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w
     const bool small = expert_counts && rp_cap < (int64_t)El * 2 * kBM;
     const bool few_tiles = rp_cap / kBM * (n_out / 256) < 4 * (int64_t)num_sms;
     const bool bn256 = n_out % 256 == 0 && !(small && few_tiles && epilogue != MOE_EPI_SILU_MUL_QUANT);
-    CUtensorMap ta, tb, to;
+    CUtensorMap ta, ta32, ta64, tb, to;
     const int o_cols = epilogue == MOE_EPI_SILU_MUL_QUANT ? n_out / 2 : n_out;
     const int o_esize = epilogue == MOE_EPI_SILU_MUL_QUANT ? 1 : epilogue == MOE_EPI_F32 ? 4 : 2;
     if (!make_tmap(&ta, a, (uint64_t)k_in, (uint64_t)rp_cap, kBM) ||
+        !make_tmap(&ta32, a, (uint64_t)k_in, (uint64_t)rp_cap, 32) ||
+        !make_tmap(&ta64, a, (uint64_t)k_in, (uint64_t)rp_cap, 64) ||
         !make_tmap(&tb, w, (uint64_t)k_in, (uint64_t)El * n_out, kBoxRows) ||
         !make_out_tmap(&to, out, (uint64_t)o_cols, (uint64_t)rp_cap, o_esize))
         return MOE_ERR_CUDA;
     switch (epilogue) {
         case MOE_EPI_SILU_MUL_QUANT:
-            return launch_tc<256, MOE_EPI_SILU_MUL_QUANT>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
+            return launch_tc<256, MOE_EPI_SILU_MUL_QUANT>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                           k_in, out, out_scale, num_sms, stream);
         case MOE_EPI_F32:
-            return bn256 ? launch_tc<256, MOE_EPI_F32>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
+            return bn256 ? launch_tc<256, MOE_EPI_F32>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                        k_in, out, out_scale, num_sms, stream)
-                         : launch_tc<128, MOE_EPI_F32>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
+                         : launch_tc<128, MOE_EPI_F32>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                        k_in, out, out_scale, num_sms, stream);
         default:
-            return bn256 ? launch_tc<256, MOE_EPI_BF16>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
+            return bn256 ? launch_tc<256, MOE_EPI_BF16>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                         k_in, out, out_scale, num_sms, stream)
-                         : launch_tc<128, MOE_EPI_BF16>(ta, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
+                         : launch_tc<128, MOE_EPI_BF16>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
                                                         k_in, out, out_scale, num_sms, stream);
     }
 }
