@@ -212,14 +212,43 @@ __global__ void __launch_bounds__(kScatterThreads)
     const int64_t wbeg = (int64_t)blockIdx.x * per_cta + (int64_t)warp * per_warp;
     const int64_t wend = min(n, wbeg + per_warp);
     int bad = 0;
-    pdl_wait();
-    pdl_trigger();
-    // the first round of this warp's slots, in flight while the histograms are summed
+    // With more than one CTA the histogram kernel ran just before this one and waited for
+    // the kernel before it before letting this one launch, so the caller's inputs are
+    // final: the ids are loaded and counted per warp (shared memory only) while the
+    // histogram kernel is still running, and this kernel waits only before its first
+    // read of the histograms. A single CTA is the scatter's first kernel and waits first.
+    const bool early = G > 1;
+    if (!early) {
+        pdl_wait();
+        pdl_trigger();
+    }
     int l0[kRound];
     load_round(ids, wbeg, wend, expert_map, E, El, lane, l0, bad);
     for (int l = threadIdx.x; l < El; l += kScatterThreads) base[l] = tot[l] = 0;
     for (int i = threadIdx.x; i < kWarps * El; i += kScatterThreads) wc[i] = 0;
     __syncthreads();
+    int32_t* mine = wc + warp * El;
+    for (int64_t r0 = wbeg; r0 < wend; r0 += 32 * kRound) {
+        int l[kRound];
+        if (r0 == wbeg) {
+#pragma unroll
+            for (int j = 0; j < kRound; ++j) l[j] = l0[j];
+        } else {
+            load_round(ids, r0, wend, expert_map, E, El, lane, l, bad);
+        }
+        // per-warp counts: equal experts of a round are aggregated first (this pass sees
+        // few slots per warp, where a hot expert would serialise per-lane atomics)
+#pragma unroll
+        for (int j = 0; j < kRound; ++j) {
+            const unsigned m = __match_any_sync(0xffffffffu, l[j]);
+            if (l[j] >= 0 && lane == __ffs(m) - 1) mine[l[j]] += __popc(m);
+            __syncwarp();
+        }
+    }
+    if (early) {
+        pdl_wait();
+        pdl_trigger();
+    }
     const bool derive = counts_in == nullptr;
     if (G > 1) {
         // per expert: sum of the earlier CTAs' histograms (and of all, when deriving the
@@ -245,24 +274,6 @@ __global__ void __launch_bounds__(kScatterThreads)
             }
             if (pre) atomicAdd(&base[l], pre);
             if (all) atomicAdd(&tot[l], all);
-        }
-    }
-    int32_t* mine = wc + warp * El;
-    for (int64_t r0 = wbeg; r0 < wend; r0 += 32 * kRound) {
-        int l[kRound];
-        if (r0 == wbeg) {
-#pragma unroll
-            for (int j = 0; j < kRound; ++j) l[j] = l0[j];
-        } else {
-            load_round(ids, r0, wend, expert_map, E, El, lane, l, bad);
-        }
-        // per-warp counts: equal experts of a round are aggregated first (this pass sees
-        // few slots per warp, where a hot expert would serialise per-lane atomics)
-#pragma unroll
-        for (int j = 0; j < kRound; ++j) {
-            const unsigned m = __match_any_sync(0xffffffffu, l[j]);
-            if (l[j] >= 0 && lane == __ffs(m) - 1) mine[l[j]] += __popc(m);
-            __syncwarp();
         }
     }
     if (derive && G == 1 && err_count) {
@@ -352,24 +363,30 @@ __global__ void __launch_bounds__(kScatterThreads)
 // the span (raw0, raw1: its bf16 bits), 8 lanes form one 1x128 group; my_dst / my_w are
 // the token's slot destinations and weights, lane k holding slot k. The row was read
 // once and is written to each kept slot.
+// the 16 bf16 values of raw0, raw1 as fp32
+__device__ __forceinline__ void unpack16(uint4 raw0, uint4 raw1, float (&v)[16]) {
+    const uint32_t w[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// have_q: the weights are not applied on the input and the caller has already quantised
+// the span (codes q0, scale s0); otherwise it is quantised here.
 template <bool kQuant>
 __device__ __forceinline__ void copy_unit(int lane, int K, int g, int col, bool active, int topk, int apply_on_input,
                                           int my_dst, float my_w, uint4 raw0, uint4 raw1, void* __restrict__ a_out,
-                                          float* __restrict__ a_scale) {
+                                          float* __restrict__ a_scale, bool have_q = false,
+                                          uint4 q0 = make_uint4(0, 0, 0, 0), float s0 = 0.f) {
     const int G = K / kGroup;
     float v[16];
-    {
-        const uint32_t w[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[2 * i] = __uint_as_float(w[i] << 16);
-            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    }
+    unpack16(raw0, raw1, v);
     if (!apply_on_input) {
-        float s = 0.f;
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (kQuant) q = quant16_group8(v, s);
+        float s = s0;
+        uint4 q = q0;
+        if (kQuant && !have_q) q = quant16_group8(v, s);
         for (int k = 0; k < topk; ++k) {
             const int d = __shfl_sync(0xffffffffu, my_dst, k);
             if (d < 0 || !active) continue;
@@ -410,31 +427,44 @@ __device__ __forceinline__ void copy_unit(int lane, int K, int g, int col, bool 
     }
 }
 
-// One warp per (token, 512-column span).
+// One warp per (token, 512-column span). The kernel before this one is always the rank
+// kernel, which waited for everything before it before letting this one launch: the
+// caller's inputs (x, the weights) are final, so the span is read (and, without the
+// weights on the input, quantised) before the wait; the destinations and every write come
+// after it.
 template <bool kQuant>
 __global__ void __launch_bounds__(256)
     scatter_copy_kernel(const uint16_t* __restrict__ x, int64_t M, int K, const int32_t* __restrict__ src2dst,
                         const float* __restrict__ topk_weights, int topk, int apply_on_input,
                         void* __restrict__ a_out, float* __restrict__ a_scale) {
     const int lane = threadIdx.x & 31;
-    pdl_wait();
-    pdl_trigger();
     const int spans = (K + 511) / 512;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (gw >= M * spans) return;
-    const int64_t t = gw / spans;
+    const bool unit = gw < M * spans;
+    const int64_t t = unit ? gw / spans : 0;
     const int g = (int)(gw % spans) * 4 + (lane >> 3);
-    const bool active = g < K / kGroup;
+    const bool active = unit && g < K / kGroup;
     const int col = g * kGroup + (lane & 7) * 16;
-    const int my_dst = lane < topk ? __ldg(src2dst + t * topk + lane) : -1;
-    const float my_w = (lane < topk && apply_on_input) ? __ldg(topk_weights + t * topk + lane) : 1.f;
+    const float my_w = (unit && lane < topk && apply_on_input) ? __ldg(topk_weights + t * topk + lane) : 1.f;
     uint4 raw0 = make_uint4(0, 0, 0, 0), raw1 = raw0;
     if (active) {
         const uint4* src = reinterpret_cast<const uint4*>(x + t * K + col);
         raw0 = __ldg(src);
         raw1 = __ldg(src + 1);
     }
-    copy_unit<kQuant>(lane, K, g, col, active, topk, apply_on_input, my_dst, my_w, raw0, raw1, a_out, a_scale);
+    uint4 q = make_uint4(0, 0, 0, 0);
+    float s = 0.f;
+    if (kQuant && !apply_on_input) {
+        float v[16];
+        unpack16(raw0, raw1, v);
+        q = quant16_group8(v, s);
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (!unit) return;
+    const int my_dst = lane < topk ? __ldg(src2dst + t * topk + lane) : -1;
+    copy_unit<kQuant>(lane, K, g, col, active, topk, apply_on_input, my_dst, my_w, raw0, raw1, a_out, a_scale,
+                      !apply_on_input, q, s);
 }
 
 // ------------------------------------------------------- scatter, small batches
