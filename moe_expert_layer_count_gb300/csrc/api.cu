@@ -317,15 +317,24 @@ int forward_chunked_impl(const void* hidden_states, const TId* topk_ids, const f
         float* sh = reinterpret_cast<float*>(ws + cv.h_scale);
         const TId* ids = topk_ids + c0 * topk;
         const float* tw = topk_weights + c0 * topk;
+        // Several chunks, each expert's rows in a chunk mostly one 128-row block: GEMM1 reads
+        // each W13 tile once per chunk, while W2 (a third of the weights) is read again by
+        // every chunk. W13 is then streamed with the L2 evict-first policy, so that it does
+        // not push W2 out of L2 between chunks.
+        const bool w13_once = M > chunk_size && cap < (int64_t)El * 2 * kGroup;
         // the chunk's expert counts come out of the scatter's own histogram pass
         int st = launch_scatter(x + c0 * K, Mc, K, ids, tw, topk, expert_map, E, El, nullptr, counts, err_count,
                                 apply_router_weight_on_input ? 1 : 0, MOE_QUANT_FP8_1X128, A, sa, offs, s2d, cap, hist, c0 > 0 ? 1 : 0, s);
         if (!st)
             st = launch_grouped_gemm(A, sa, w13, w13_scale, offs, counts, El, cap, 2 * N, K, MOE_EPI_SILU_MUL_QUANT, H, sh,
-                                     sms, s);
+                                     sms, s, w13_once ? kOptWeightsEvictFirst : 0);
         if (!st)
             st = launch_grouped_gemm(H, sh, w2, w2_scale, offs, counts, El, cap, K, N, MOE_EPI_BF16, Y, nullptr, sms, s);
-        if (!st) st = launch_gather(Y, s2d, tw, Mc, topk, K, apply_router_weight_on_input ? 1 : 0, o + c0 * K, s);
+        // the next chunk's one-kernel scatter ranks its slots while this chunk's gather runs
+        const int64_t next = M - c0 - Mc;
+        const int early_next = next > 0 && scatter_is_one_kernel(next < chunk_size ? next : chunk_size, topk, El);
+        if (!st)
+            st = launch_gather(Y, s2d, tw, Mc, topk, K, apply_router_weight_on_input ? 1 : 0, o + c0 * K, s, early_next);
         if (st) return st;
     }
     return MOE_OK;

@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                    const __grid_constant__ CUtensorMap tmA64, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, const float* __restrict__ sa, const float* __restrict__ sw,
                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts,
-                   int El, int row_cap, int n_out, int k_in, void* __restrict__ out, float* __restrict__ out_scale) {
+                   int El, int row_cap, int n_out, int k_in, void* __restrict__ out, float* __restrict__ out_scale,
+                   int opts) {
     using C = Cfg<BN, EPI>;
     constexpr bool kSilu = EPI == MOE_EPI_SILU_MUL_QUANT;
     constexpr bool kStaged = staged_scales<EPI>();
@@ -244,6 +245,9 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
+            // (the plain load measured faster than the hinted one with the normal priority)
+            const bool w_evict_first = (opts & kOptWeightsEvictFirst) != 0;
+            const uint64_t w_policy = ptx::policy_evict_first();
             for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
                 const int mt = tile / n_tiles, nt = tile % n_tiles;
                 const int row0 = mt * kBM;
@@ -275,7 +279,10 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                             brow = l * n_out + (p & 1) * (n_out / 2) + nt * 128 + (p >> 1) * kBoxRows;
                         else
                             brow = l * n_out + nt * BN + p * kBoxRows;
-                        ptx::tma_load_2d(b_dst + p * kBoxRows * kBK, &tmB, kb * kBK, brow, full);
+                        if (w_evict_first)
+                            ptx::tma_load_2d_hint(b_dst + p * kBoxRows * kBK, &tmB, kb * kBK, brow, full, w_policy);
+                        else
+                            ptx::tma_load_2d(b_dst + p * kBoxRows * kBK, &tmB, kb * kBK, brow, full);
                     }
                 }
             }
@@ -624,7 +631,7 @@ template <int BN, int EPI, bool kSkip>
 int launch_tc_k(const CUtensorMap& ta, const CUtensorMap& ta32, const CUtensorMap& ta64, const CUtensorMap& tb, const CUtensorMap& to,
                 const float* a_scale,
                 const float* w_scale, const int32_t* offsets, const int32_t* counts, int El, int64_t rp_cap,
-                int n_out, int k_in, void* out, float* out_scale, int num_sms, cudaStream_t stream) {
+                int n_out, int k_in, void* out, float* out_scale, int num_sms, cudaStream_t stream, int opts) {
     const size_t smem = smem_bytes<BN, EPI>(El);
     // the shared-memory opt-in is a property of the kernel in each device's context: set
     // it once per device (racing first calls only set the same value twice)
@@ -642,7 +649,7 @@ int launch_tc_k(const CUtensorMap& ta, const CUtensorMap& ta32, const CUtensorMa
     const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid < 1) return MOE_OK;
     launch_k(gemm_tc_kernel<BN, EPI, kSkip>, grid, threads_of<EPI>(), smem, stream, ta, ta32, ta64, tb, to, a_scale, w_scale,
-             offsets, counts, El, (int)rp_cap, n_out, k_in, out, out_scale);
+             offsets, counts, El, (int)rp_cap, n_out, k_in, out, out_scale, opts);
     note_launches(1);
     return launch_status();
 }
@@ -654,12 +661,12 @@ template <int BN, int EPI>
 int launch_tc(const CUtensorMap& ta, const CUtensorMap& ta32, const CUtensorMap& ta64, const CUtensorMap& tb, const CUtensorMap& to,
               const float* a_scale,
               const float* w_scale, const int32_t* offsets, const int32_t* counts, int El, int64_t rp_cap, int n_out,
-              int k_in, void* out, float* out_scale, int num_sms, cudaStream_t stream) {
+              int k_in, void* out, float* out_scale, int num_sms, cudaStream_t stream, int opts) {
     if (counts && rp_cap < (int64_t)El * 2 * kBM)
         return launch_tc_k<BN, EPI, true>(ta, ta32, ta64, tb, to, a_scale, w_scale, offsets, counts, El, rp_cap, n_out, k_in, out,
-                                          out_scale, num_sms, stream);
+                                          out_scale, num_sms, stream, opts);
     return launch_tc_k<BN, EPI, false>(ta, ta32, ta64, tb, to, a_scale, w_scale, offsets, counts, El, rp_cap, n_out, k_in, out,
-                                       out_scale, num_sms, stream);
+                                       out_scale, num_sms, stream, opts);
 }
 
 }  // namespace
@@ -667,7 +674,7 @@ int launch_tc(const CUtensorMap& ta, const CUtensorMap& ta32, const CUtensorMap&
 int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
                         const int32_t* expert_offsets, const int32_t* expert_counts, int El, int64_t rp_cap, int n_out,
                         int k_in, int epilogue,
-                        void* out, float* out_scale, int num_sms, cudaStream_t stream) {
+                        void* out, float* out_scale, int num_sms, cudaStream_t stream, int opts) {
     if (rp_cap == 0) return MOE_OK;
     // 256-wide tiles, except for a bf16/fp32 output of a small batch whose 256-wide tiles
     // would fill fewer than four waves of the SMs (a 128-token chunk: ~3 waves, the last
@@ -687,17 +694,17 @@ int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w
     switch (epilogue) {
         case MOE_EPI_SILU_MUL_QUANT:
             return launch_tc<256, MOE_EPI_SILU_MUL_QUANT>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
-                                                          k_in, out, out_scale, num_sms, stream);
+                                                          k_in, out, out_scale, num_sms, stream, opts);
         case MOE_EPI_F32:
             return bn256 ? launch_tc<256, MOE_EPI_F32>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
-                                                       k_in, out, out_scale, num_sms, stream)
+                                                       k_in, out, out_scale, num_sms, stream, opts)
                          : launch_tc<128, MOE_EPI_F32>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
-                                                       k_in, out, out_scale, num_sms, stream);
+                                                       k_in, out, out_scale, num_sms, stream, opts);
         default:
             return bn256 ? launch_tc<256, MOE_EPI_BF16>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
-                                                        k_in, out, out_scale, num_sms, stream)
+                                                        k_in, out, out_scale, num_sms, stream, opts)
                          : launch_tc<128, MOE_EPI_BF16>(ta, ta32, ta64, tb, to, a_scale, w_scale, expert_offsets, expert_counts, El, rp_cap, n_out,
-                                                        k_in, out, out_scale, num_sms, stream);
+                                                        k_in, out, out_scale, num_sms, stream, opts);
     }
 }
 

@@ -474,10 +474,10 @@ __global__ void __launch_bounds__(256)
 // __match_any_sync), then copies and quantises its own (token, span) units. Ranking a few
 // thousand slots costs each CTA far less than the launch and the global round trip of a
 // separate index kernel. CTA 0 writes the offsets, counts and src2dst.
-// early != 0 (only for chunks after the first inside the chunk loop, where the kernel
-// still running before this one is the previous chunk's gather, which touches none of
-// these inputs): the ids, expert map, weights and the unit's row are read and ranked
-// before waiting for that kernel; every write still comes after the wait.
+// early != 0 (only for chunks after the first inside the chunk loop, where the kernels
+// still running before this one are the previous chunk's GEMMs and gather, none of which
+// writes these inputs): the ids, expert map, weights and the unit's row are read and
+// ranked before waiting for them; every write still comes after the wait.
 constexpr int kSmallSlots = 4096;
 constexpr int kSmallGroups = kSmallSlots / (kScatterThreads / 32) / 32;  // groups of 32 per warp at most
 
@@ -620,6 +620,11 @@ __global__ void __launch_bounds__(kScatterThreads)
     copy_unit<kQuant>(lane, K, g, col, active, topk, apply_on_input, my_dst, my_w, raw0, raw1, a_out, a_scale);
 }
 
+bool scatter_is_one_kernel(int64_t M, int topk, int El) {
+    const int64_t n = M * topk;
+    return n <= kSmallSlots && (size_t)(El + 1 + (kScatterThreads / 32) * El + n) * sizeof(int32_t) <= 48 * 1024;
+}
+
 template <typename TId>
 int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const float* topk_weights, int topk,
                    const int32_t* expert_map, int E, int El, const int32_t* counts_in, int32_t* counts_out,
@@ -628,8 +633,8 @@ int launch_scatter(const uint16_t* x, int64_t M, int K, const TId* ids, const fl
                    cudaStream_t stream) {
     const int64_t n = M * topk;
     const int row_cap = (int)(rp_cap / kGroup * kGroup);
-    const size_t small_smem = (size_t)(El + 1 + (kScatterThreads / 32) * El + n) * sizeof(int32_t);
-    if (n <= kSmallSlots && small_smem <= 48 * 1024) {
+    if (scatter_is_one_kernel(M, topk, El)) {
+        const size_t small_smem = (size_t)(El + 1 + (kScatterThreads / 32) * El + n) * sizeof(int32_t);
         const int64_t units = M * ((K + 511) / 512);
         const unsigned sgrid = (unsigned)(units > 0 ? (units + 7) / 8 : 1);
         const size_t smem = small_smem;
@@ -684,10 +689,14 @@ MOE_INSTANTIATE_SCATTER(int64_t)
 __global__ void __launch_bounds__(256)
     gather_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ src2dst,
                   const float* __restrict__ topk_weights, int64_t M, int topk, int K, int apply_on_input,
-                  uint16_t* __restrict__ out) {
+                  uint16_t* __restrict__ out, int early_trigger) {
     const int lane = threadIdx.x & 31;
+    // early_trigger (inside a chunk loop, when the next chunk's one-kernel scatter follows,
+    // which reads only the call's own inputs before its own wait): the next kernel may
+    // launch at once, and ranks its slots while this one runs.
+    if (early_trigger) pdl_trigger();
     pdl_wait();
-    pdl_trigger();
+    if (!early_trigger) pdl_trigger();
     const int spans = (K + 255) / 256;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (gw >= M * spans) return;
@@ -730,10 +739,11 @@ __global__ void __launch_bounds__(256)
 }
 
 int launch_gather(const uint16_t* y, const int32_t* src2dst, const float* topk_weights, int64_t M, int topk, int K,
-                  int apply_on_input, uint16_t* out, cudaStream_t stream) {
+                  int apply_on_input, uint16_t* out, cudaStream_t stream, int early_trigger) {
     if (M == 0) return MOE_OK;
     const int64_t warps = M * ((K + 255) / 256);
-    launch_k(gather_kernel, (unsigned)((warps + 7) / 8), 256, 0, stream, y, src2dst, topk_weights, M, topk, K, apply_on_input, out);
+    launch_k(gather_kernel, (unsigned)((warps + 7) / 8), 256, 0, stream, y, src2dst, topk_weights, M, topk, K, apply_on_input,
+             out, early_trigger);
     note_launches(1);
     return launch_status();
 }
