@@ -257,7 +257,8 @@ MOE_API int moe_gather_weight_reduce(const void* y, const int32_t* src2dst, cons
  *   hidden_states bf16 [M, K];  topk_ids int32 [M, topk];  topk_weights fp32 [M, topk]
  *   w13 e4m3 [El, 2N, K] (gate rows then up rows), w13_scale fp32 [El, 2N/128, K/128]
  *   w2  e4m3 [El, K, N],  w2_scale fp32 [El, K/128, N/128]
- *   out bf16 [M, K], must not overlap the workspace
+ *   out bf16 [M, K]; it may be hidden_states itself (in place) but must not otherwise
+ *       overlap hidden_states, topk_ids, topk_weights or the workspace
  *   workspace >= moe_workspace_size(min(chunk_size, M), K, N, topk, El) bytes
  *   err_count int32 [1] or NULL (bad ids are added)
  * The result of every row depends only on its own chunk, and the GEMM tiling does not

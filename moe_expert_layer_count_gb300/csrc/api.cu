@@ -285,11 +285,19 @@ int forward_chunked_impl(const void* hidden_states, const TId* topk_ids, const f
     const int El = local_num_experts;
     const int64_t cmax = chunk_size < M ? chunk_size : M;
     if (workspace_bytes < moe_workspace_size(cmax, K, N, topk, El)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-    // out must not overlap the workspace
+    // out must not overlap the workspace, nor the inputs, except hidden_states exactly
+    // (in place: each chunk reads its own rows of hidden_states, and the next chunk's
+    // scatter reads its rows while this chunk's gather still writes)
     {
         const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), o1 = o0 + (size_t)M * K * 2;
-        const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), w1 = w0 + workspace_bytes;
-        if (o0 < w1 && w0 < o1) return MOE_ERR_INVALID_ARG;
+        auto hits = [&](const void* p, size_t bytes) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+            return o0 < a + bytes && a < o1;
+        };
+        if (hits(workspace, workspace_bytes) || hits(topk_ids, (size_t)M * topk * sizeof(TId)) ||
+            hits(topk_weights, (size_t)M * topk * sizeof(float)) ||
+            (out != hidden_states && hits(hidden_states, (size_t)M * K * 2)))
+            return MOE_ERR_INVALID_ARG;
     }
     if ((reinterpret_cast<uintptr_t>(hidden_states) | reinterpret_cast<uintptr_t>(out) |
          reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(w13) | reinterpret_cast<uintptr_t>(w2)) &

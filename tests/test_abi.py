@@ -68,6 +68,12 @@ def test_argument_checks_return_before_any_launch(L):
     # workspace too small
     assert L.moe_forward_chunked(p, p, p, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 4, 0, p,
                                  ws, 16, None, None) == 2
+    # out overlapping hidden_states other than exactly, or the top-k ids / weights
+    x, ids, tw = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)
+    big = ctypes.c_void_p(1 << 40)
+    for out in (ctypes.c_void_p((1 << 20) + 256), ids, ctypes.c_void_p((3 << 20) - 16)):
+        assert L.moe_forward_chunked(x, ids, tw, p, p, p, p, None, 8, 8, 4, 128, 128, 2, 4, 0, out,
+                                     big, 1 << 30, None, None) == 1
     # the int64-id twins run the same checks
     assert L.moe_count_expert_tokens_i64(p, 4, 0, None, 8, 8, p, None, None) == 1      # topk 0
     assert L.moe_scatter_i64(p, 4, 100, p, p, 2, None, 8, 8, p, 0, None, 0, 1, p, p, p, p, 1 << 20, p,
