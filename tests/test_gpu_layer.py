@@ -203,6 +203,25 @@ def test_tiny_layer_chunk_sizes_bit_identical(tiny):
         assert (gpu_forward(d, li.wl.E, chunk=chunk) == full).all(), chunk
 
 
+def test_layer_in_place_equals_separate_output():
+    """out may be hidden_states itself: every chunk reads only its own rows before its
+    gather writes them, also while the next chunk's scatter reads ahead. Several chunks of
+    the one-kernel scatter (128-token chunks) and of the three-kernel one (1024)."""
+    wl = mi.QWEN3_DECODE
+    for M, chunk in ((1000, 128), (3000, 1024)):
+        ids, tw = mi.route(M, wl.E, wl.topk, 41, 1.2)
+        x = mi.hidden_states(M, wl.K, 41)
+        li = mi.make_layer_inputs(wl)
+        w = (dev(li.w13), dev(li.w13_scale), dev(li.w2), dev(li.w2_scale))
+        d_ids, d_tw = dev(ids), dev(tw)
+        ref = moe.moe_forward_chunked(dev(x), d_ids, d_tw, *w, wl.E, chunk_size=chunk)
+        xin = dev(x)
+        got = moe.moe_forward_chunked(xin, d_ids, d_tw, *w, wl.E, chunk_size=chunk, out=xin)
+        torch.cuda.synchronize()
+        assert got.data_ptr() == xin.data_ptr()
+        assert (host_bits(got) == host_bits(ref)).all(), (M, chunk)
+
+
 def test_tiny_layer_local_experts(tiny):
     li, d = tiny
     E = li.wl.E
