@@ -29,6 +29,8 @@
 // Small batches (given the experts' valid row counts) run a variant in which an epilogue
 // warp whose 32 rows are all padding skips the TMEM reads, folding and stores, and in
 // which a tile whose kept rows all lie in its first 32 (or 64) loads only those rows of A.
+// With kOptWeightsEvictFirst the weight tiles are loaded under the L2 evict-first policy
+// (the chunk loop sets it for W13 when every chunk reads each W13 tile once).
 // Every wait on a pipeline barrier gives up after 2 s, sets a device error word and an
 // abort flag seen by all roles, waits (bounded) for its own copies and MMAs in flight,
 // and the CTA frees its TMEM and returns. An epilogue warp that gives up arrives on the
@@ -245,7 +247,8 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            // (the plain load measured faster than the hinted one with the normal priority)
+            // weight tiles take the cache-hinted load only under kOptWeightsEvictFirst (the
+            // plain load measured faster than a hinted one at the normal priority)
             const bool w_evict_first = (opts & kOptWeightsEvictFirst) != 0;
             const uint64_t w_policy = ptx::policy_evict_first();
             for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {

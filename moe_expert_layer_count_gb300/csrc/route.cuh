@@ -43,16 +43,16 @@ int launch_gather(const uint16_t* y, const int32_t* src2dst, const float* topk_w
 int launch_silu_mul_quant(const float* c1, const int32_t* expert_offsets, int El, int64_t rp_cap, int N, uint8_t* h,
                           float* h_scale, cudaStream_t stream);
 
-// expert_counts (nullable): valid rows of each expert's block; rows past them are
-// padding, and 32-row groups made only of padding are neither computed nor stored.
 // Options of launch_grouped_gemm (bits of opts):
 //  kOptWeightsEvictFirst: the weight tiles are loaded with the L2 evict-first policy.
 constexpr int kOptWeightsEvictFirst = 1;
+
+// expert_counts (nullable): valid rows of each expert's block; rows past them are
+// padding, and 32-row groups made only of padding are neither computed nor stored.
 int launch_grouped_gemm(const uint8_t* a, const float* a_scale, const uint8_t* w, const float* w_scale,
                         const int32_t* expert_offsets, const int32_t* expert_counts, int El, int64_t rp_cap,
                         int n_out, int k_in, int epilogue, void* out, float* out_scale, int num_sms,
-                        cudaStream_t stream,
-                        int opts = 0);
+                        cudaStream_t stream, int opts = 0);
 
 // moe_forward_chunked for either top-k id type (the argument checks included).
 template <typename TId>
