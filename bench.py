@@ -181,9 +181,10 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------ our arm
 def run_count_only(args, world, local_rank):
-    """The count step alone (count_expert_num_tokens) over 2^20 tokens of top-8 ids. The
-    ids (33.5 MB) fit in L2, so L2 is flushed (a 256 MB write) before every timed step and
-    each step is timed by its own events."""
+    """The count step alone (count_expert_num_tokens) over 2^20 (or 2^23) tokens of top-8
+    ids. 2^20 tokens of ids (33.5 MB) fit in L2, so L2 is flushed (a 256 MB write) before
+    every timed step; 2^23 (268 MB) exceed it and need no flush. Each step is timed by its
+    own events."""
     import torch
 
     import moe_expert_layer_count_gb300 as moe
@@ -191,11 +192,12 @@ def run_count_only(args, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = mi.WORKLOADS[args.workload]
-    ids_np, _ = mi.route(wl.M, wl.E, wl.topk, wl.seed, wl.zipf_s)
+    ids_np, _ = mi.count_only_routing(wl)
     ids = torch.from_numpy(ids_np).to(dev)
+    flush_l2 = ids_np.nbytes < (200 << 20)
     cnt = torch.empty(wl.El, dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20 if flush_l2 else 1, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(i_ids=ids):
@@ -211,7 +213,8 @@ def run_count_only(args, world, local_rank):
     l0 = moe.moe_kernel_launch_count()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for e0, e1 in evs:
-        flush.zero_()
+        if flush_l2:
+            flush.zero_()
         e0.record(stream)
         step()
         e1.record(stream)
@@ -606,9 +609,11 @@ def workload_config(wl, world):
     c.update({"experts": wl.E, "local_experts": wl.El, "topk": wl.topk, "chunk_size": wl.chunk,
               "routing": f"zipf s={wl.zipf_s}" if wl.zipf_s else "uniform",
               "parallelism": f"replicas x{world} (one independent batch per GPU)"})
-    if wl.name == mi.COUNT_ONLY.name:
+    if mi.is_count_only(wl):
         c["step"] = "count only"
-        c["l2"] = "flushed before every timed step (256 MB write); each step timed by its own events"
+        c["l2"] = ("flushed before every timed step (256 MB write); each step timed by its own events"
+                   if wl.M * wl.topk * 4 < (200 << 20) else
+                   "inputs larger than L2 (268 MB of ids, the 2^20-token routing repeated 8 times); no flush")
     elif wl.N:
         c["l2"] = "inputs larger than L2: the touched experts' FP8 weights alone exceed the 129 MB L2"
     else:
@@ -621,9 +626,9 @@ ORACLE_BUDGET_S = 90.0  # wall time the reference arm's timed + warm-up oracle c
 
 
 def _oracle_inputs(wl):
-    count_only = wl.name == mi.COUNT_ONLY.name
+    count_only = mi.is_count_only(wl)
     if count_only:  # only the routing is needed
-        ids, w = mi.route(wl.M, wl.E, wl.topk, wl.seed, wl.zipf_s)
+        ids, w = mi.count_only_routing(wl)
         return mi.LayerInputs(wl, np.zeros((wl.M, 0), np.uint16), ids, w, None)
     return mi.make_layer_inputs(wl)
 
@@ -632,7 +637,7 @@ def _oracle_call(wl, li, m, parallel):
     """One oracle pass over the first m tokens of the workload (the OpenMP build when
     parallel; only the layer has a multi-threaded row loop)."""
     import oracle
-    if wl.name == mi.COUNT_ONLY.name:
+    if mi.is_count_only(wl):
         oracle.count(li.topk_ids[:m], wl.E, wl.El)
     elif wl.N:
         oracle.forward_chunked(li.x[:m], li.topk_ids[:m], li.topk_weights[:m], li.w13, li.w13_scale, li.w2,
@@ -675,7 +680,7 @@ def cpu_baseline(wl, calls):
     reported value) and the single-threaded checker, on the reference arm's sample."""
     import oracle
     li, m = oracle_sample(wl, calls)
-    par = bool(wl.N) and wl.name != mi.COUNT_ONLY.name
+    par = bool(wl.N) and not mi.is_count_only(wl)
     v, n, t = _timed(wl, li, m, par, 8.0)
     v1, n1, t1 = _timed(wl, li, m, False, 8.0)
     cores = oracle.num_threads(True) if par else 1
@@ -692,7 +697,7 @@ def run_reference(args):
     import oracle
     wl = mi.WORKLOADS[args.workload]
     li, m = oracle_sample(wl, args.warmup + args.steps)
-    par = bool(wl.N) and wl.name != mi.COUNT_ONLY.name
+    par = bool(wl.N) and not mi.is_count_only(wl)
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
@@ -728,7 +733,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    if args.workload == mi.COUNT_ONLY.name:
+    if mi.is_count_only(mi.WORKLOADS[args.workload]):
         line = run_count_only(args, world, local_rank)
     else:
         line = run_ours(args, rank, world, local_rank)

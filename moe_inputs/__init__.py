@@ -70,8 +70,16 @@ QWEN3_CHUNKED = Workload("qwen3_30b_a3b_chunked_m16385_c128_local64_zipf1.2", M=
                          local_experts=64, chunk_size=128)
 COUNT_ONLY = Workload("count_only_m1048576_e128_top8", M=1 << 20, K=128, N=0, E=128, topk=8,
                       seed=6)
+# The same count pass over 2^23 tokens (268 MB of ids, twice the L2): its ids are the 2^20
+# routing repeated eight times, so every step streams them from DRAM without an L2 flush.
+COUNT_ONLY_LARGE = Workload("count_only_m8388608_e128_top8", M=1 << 23, K=128, N=0, E=128,
+                            topk=8, seed=6)
 WORKLOADS = {w.name: w for w in (TINY, PERMUTE_ONLY, QWEN3_DECODE, QWEN3_PREFILL,
-                                 QWEN3_CHUNKED, COUNT_ONLY)}
+                                 QWEN3_CHUNKED, COUNT_ONLY, COUNT_ONLY_LARGE)}
+
+
+def is_count_only(wl: Workload) -> bool:
+    return wl.name in (COUNT_ONLY.name, COUNT_ONLY_LARGE.name)
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -113,6 +121,16 @@ def route(M: int, E: int, topk: int, seed: int, zipf_s: float = 0.0):
     w = np.take_along_axis(probs, ids, axis=1).astype(np.float32)
     w = (w / w.sum(axis=1, keepdims=True, dtype=np.float32)).astype(np.float32)
     return np.ascontiguousarray(ids), np.ascontiguousarray(w)
+
+
+def count_only_routing(wl: Workload):
+    """The count-only workloads' top-k ids and weights: the 2^20-token routing of the
+    workload's seed, repeated to the workload's M (a multiple of 2^20)."""
+    ids, w = route(COUNT_ONLY.M, wl.E, wl.topk, wl.seed, wl.zipf_s)
+    reps = wl.M // COUNT_ONLY.M
+    if reps <= 1:
+        return ids, w
+    return np.ascontiguousarray(np.tile(ids, (reps, 1))), np.ascontiguousarray(np.tile(w, (reps, 1)))
 
 
 def expert_map(E: int, local: Optional[int]) -> Optional[np.ndarray]:
