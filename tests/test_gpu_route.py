@@ -192,6 +192,26 @@ def test_gather_bit_exact(M, topk, K, drop, apply_on_input):
     assert (host_bits(out) == ref).all()
 
 
+def test_gather_reduction_order_and_rounding():
+    """The two hand-worked reductions of the oracle's pins, on the kernel: rows 1, 2^-24,
+    -1 summed in ascending k give 0 (in descending order 2^-24), and a weighted row whose
+    exact product lies just above 2^-24 still gives 0 because the product is rounded to
+    fp32 before the add."""
+    K = 128
+    y1 = np.float32(2.0 ** -24 * (1 + 2.0 ** -7))
+    w1 = np.float32(0.9922481179237366)
+    Y = np.zeros((4, K), np.float32)
+    Y[0, 0], Y[1, 0], Y[2, 0], Y[3, 0] = 1.0, 2.0 ** -24, -1.0, y1
+    s2d = np.array([[0, 1, 2], [2, 1, 0], [0, 3, 2]], np.int32)
+    w = np.array([[1, 1, 1], [1, 1, 1], [1, w1, 1]], np.float32)
+    out = moe.moe_gather_weight_reduce(dev(mi.bf16_bits(Y)), dev(s2d), dev(w))
+    torch.cuda.synchronize()
+    got = mi.bf16_to_f32(host_bits(out))[:, 0]
+    assert list(got) == [0.0, np.float32(2.0 ** -24), 0.0]
+    ref = mi.bf16_to_f32(oracle.gather(mi.bf16_bits(Y), s2d, w))[:, 0]
+    assert (got == ref).all()
+
+
 @pytest.mark.parametrize("N,counts", [(128, [3, 0, 130]), (768, [1, 64, 5, 0, 200])])
 def test_silu_mul_quant(N, counts):
     rng = np.random.default_rng(N)

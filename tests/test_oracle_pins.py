@@ -302,6 +302,35 @@ def test_gather_weights_and_dropped_slots():
     assert list(out[0]) == [2.5, -1.25] and list(out[1]) == [0.0, 0.0]
 
 
+def test_gather_sums_in_fp32_in_ascending_k():
+    """Reading C8: the weighted rows are added in fp32 in ascending k. Rows 1, 2^-24, -1
+    with weights 1: in ascending fp32 order 1 + 2^-24 rounds to 1 (a tie, to even) and
+    the sum is 0; any other order (or an fp64 or pairwise sum) gives 2^-24."""
+    Y = mi.bf16_bits(np.array([[1.0, 0.0], [2.0 ** -24, 0.0], [-1.0, 0.0]], np.float32))
+    w = np.ones((1, 3), np.float32)
+    assert mi.bf16_to_f32(oracle.gather(Y, np.array([[0, 1, 2]], np.int32), w))[0, 0] == 0.0
+    # the same rows in descending order: -1 + 2^-24 is exact in fp32, + 1 leaves 2^-24
+    assert mi.bf16_to_f32(oracle.gather(Y, np.array([[2, 1, 0]], np.int32), w))[0, 0] == np.float32(2.0 ** -24)
+
+
+def test_gather_rounds_product_and_sum_separately():
+    """Reading C8: each weighted row is rounded to fp32 before it is added (no fused
+    multiply-add). The second product p = w1 * y1 lies just above 2^-24 (half an ulp of
+    1.0) and rounds to exactly 2^-24, so 1 + fl(p) is a tie that rounds to 1 and the
+    third row (-1) leaves 0; a fused 1 + p would round up to 1 + 2^-23 and leave 2^-23."""
+    from fractions import Fraction
+    y1 = np.float32(2.0 ** -24 * (1 + 2.0 ** -7))   # a bf16 value
+    w1 = np.float32(0.9922481179237366)             # one fp32 step above 1/(1 + 2^-7)
+    p = Fraction(float(w1)) * Fraction(float(y1))
+    half_ulp = Fraction(2) ** -24
+    assert half_ulp < p < half_ulp * (1 + Fraction(2) ** -24)   # exact product just above the tie
+    assert np.float32(w1) * np.float32(y1) == np.float32(2.0 ** -24)
+    Y = mi.bf16_bits(np.array([[1.0, 0.0], [float(y1), 0.0], [-1.0, 0.0]], np.float32))
+    assert mi.bf16_to_f32(Y)[1, 0] == y1
+    w = np.array([[1.0, w1, 1.0]], np.float32)
+    assert mi.bf16_to_f32(oracle.gather(Y, np.array([[0, 1, 2]], np.int32), w))[0, 0] == 0.0
+
+
 # --------------------------------------------------------------------------- GEMMs
 def _dequant_weights(W, S):
     El, R, C = W.shape
