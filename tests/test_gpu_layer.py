@@ -222,6 +222,32 @@ def test_layer_in_place_equals_separate_output():
         assert (host_bits(got) == host_bits(ref)).all(), (M, chunk)
 
 
+def test_layer_chunk_sizes_mix_scatter_forms_bit_identical():
+    """Chunk sizes whose chunks take different scatter forms give the same output bit for
+    bit: one chunk of 8800 slots (three-kernel scatter), chunks of 600 tokens (three-kernel,
+    then a last chunk of 500 tokens = 4000 slots in the one-kernel form), chunks of 512
+    (4096 slots, the one-kernel form's limit) and of 100 (one-kernel, the gather of each
+    chunk launching the next chunk's scatter early)."""
+    wl = mi.QWEN3_DECODE
+    M = 1100
+    ids, tw = mi.route(M, wl.E, wl.topk, 77, 1.2)
+    x = dev(mi.hidden_states(M, wl.K, 77))
+    li = mi.make_layer_inputs(wl)
+    w = (dev(li.w13), dev(li.w13_scale), dev(li.w2), dev(li.w2_scale))
+    d_ids, d_tw = dev(ids), dev(tw)
+    outs = {}
+    for chunk in (None, 600, 512, 100):
+        out = moe.moe_forward_chunked(x, d_ids, d_tw, *w, wl.E, chunk_size=chunk)
+        torch.cuda.synchronize()
+        outs[chunk] = host_bits(out)
+    for chunk in (600, 512, 100):
+        assert (outs[chunk] == outs[None]).all(), chunk
+    toks = np.array([0, 1, 599, 600, 1023, 1099])
+    ref = oracle.forward_tokens(toks, mi.hidden_states(M, wl.K, 77), ids, tw, li.w13, li.w13_scale, li.w2,
+                                li.w2_scale, wl.E)
+    layer_tolerance(outs[None][toks], ref)
+
+
 def test_tiny_layer_local_experts(tiny):
     li, d = tiny
     E = li.wl.E
