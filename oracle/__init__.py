@@ -1,7 +1,7 @@
 """CPU oracle of the fused-MoE layer hot path -- TEST INFRASTRUCTURE ONLY.
 
-Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may
-import this package. The CUDA path never imports it, and it imports nothing from the
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg and
+reference arm may import this package. The CUDA path never imports it, and it imports nothing from the
 CUDA path: the two share only the seeded input generators of ``moe_inputs``.
 
 The arithmetic lives in ``moe_oracle.c`` (plain C, built with gcc by ``build.py``);

@@ -2,7 +2,7 @@
  * moe_oracle.c -- plain, slow CPU oracle of the fused-MoE layer hot path.
  *
  * TEST INFRASTRUCTURE ONLY. Only the test suite, the package smoke check and the
- * benchmark's CPU-baseline leg may load this file's library. It shares no code, header,
+ * benchmark's CPU-baseline leg and reference arm may load this file's library. It shares no code, header,
  * table or constant with the CUDA path, and the CUDA path never calls it.
  *
  * What is computed follows three vLLM pull-request pages:
